@@ -1,0 +1,116 @@
+"""Seeded synthetic inputs for the Beam routed-MoE layer.
+
+This module holds the layer shapes and the seeded random draws that feed both the CUDA
+library and the CPU oracle. It holds none of the method's arithmetic: no routing, no
+activation, no reduction. Every tensor is drawn from its own generator, seeded from
+(seed, tensor tag), so two workloads that share a seed share their weights whatever their
+token count.
+
+Shapes come from the Beam release pages:
+  * "Reflection releases Beam, a 501B open MoE model with 1M context", Architecture
+    paragraph: hidden size 5,120; 256 experts per MoE layer in 8 groups of 32; the 4 best
+    groups are kept; 8 experts per token; SwiGLU experts of intermediate size 2,560;
+    outputs scaled by 2.5.
+  * transformers "Beam" model doc, Overview, "Sparse MoE" bullet: the config names
+    n_group, topk_group and routed_scaling_factor.
+
+Value distributions (the pages give none; these are the synthetic recipe):
+  x ~ N(0, 1) rounded to BF16; router weight ~ N(0, 0.02^2) FP32; expert bias ~ U(-0.1, 0.1)
+  FP32; gate/up ~ N(0, 1/d) and down ~ N(0, 1/I), both rounded to BF16 (std 1/sqrt(fan_in)).
+  The skewed-load workload adds +0.5 to the bias of 16 seeded "hot" experts.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class MoEShape:
+    """Shape of one routed-MoE layer (names follow the transformers BeamConfig fields)."""
+
+    d: int = 5120            # hidden size
+    I: int = 2560            # expert intermediate size
+    E: int = 256             # routed experts
+    n_group: int = 8         # expert groups
+    topk_group: int = 4      # groups kept per token
+    top_k: int = 8           # experts per token
+    scale: float = 2.5       # routed_scaling_factor
+
+
+BEAM = MoEShape()
+TINY = MoEShape(d=512, I=256)
+
+# Tags that decorrelate the per-tensor generators.
+_TAG = {"x": 1, "router_w": 2, "bias": 3, "w_gate": 4, "w_up": 5, "w_down": 6, "hot": 7, "sample": 8}
+
+
+def generator(seed: int, tag: str, device: str | torch.device = "cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000 + _TAG[tag])
+    return g
+
+
+def make_tokens(shape: MoEShape, T: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """x [T, d] BF16, N(0, 1)."""
+    g = generator(seed, "x", device)
+    return torch.randn((T, shape.d), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def make_router(shape: MoEShape, seed: int = 0, device="cpu", hot_experts: int = 0, hot_bias: float = 0.5):
+    """Router weight [E, d] FP32 ~ N(0, 0.02^2) and expert bias [E] FP32 ~ U(-0.1, 0.1).
+
+    With hot_experts > 0, that many experts (a seeded permutation's first entries) get
+    +hot_bias on top of their bias, which skews the per-expert load.
+    """
+    g = generator(seed, "router_w", device)
+    w = torch.randn((shape.E, shape.d), generator=g, device=device, dtype=torch.float32).mul_(0.02)
+    gb = generator(seed, "bias", device)
+    b = torch.rand((shape.E,), generator=gb, device=device, dtype=torch.float32).mul_(0.2).sub_(0.1)
+    if hot_experts:
+        hot = hot_expert_ids(shape, hot_experts, seed)
+        b[hot.to(device)] += hot_bias
+    return w, b
+
+
+def hot_expert_ids(shape: MoEShape, n: int, seed: int = 0) -> torch.Tensor:
+    g = generator(seed, "hot", "cpu")
+    return torch.randperm(shape.E, generator=g)[:n]
+
+
+def make_experts(shape: MoEShape, seed: int = 0, device="cpu"):
+    """w_gate, w_up [E, I, d] and w_down [E, d, I], BF16, std 1/sqrt(fan_in).
+
+    Drawn one expert at a time in FP32, scaled, then rounded to BF16, so the peak extra
+    memory is one expert matrix in FP32.
+    """
+    E, d, I = shape.E, shape.d, shape.I
+    out = []
+    for tag, rows, fan_in in (("w_gate", I, d), ("w_up", I, d), ("w_down", d, I)):
+        g = generator(seed, tag, device)
+        w = torch.empty((E, rows, fan_in), device=device, dtype=torch.bfloat16)
+        std = 1.0 / math.sqrt(fan_in)
+        for e in range(E):
+            w[e].copy_(torch.randn((rows, fan_in), generator=g, device=device, dtype=torch.float32).mul_(std))
+        out.append(w)
+    return tuple(out)
+
+
+def sample_tokens(T: int, n: int, seed: int = 0) -> torch.Tensor:
+    """A seeded, sorted subset of n distinct token indices out of T (all of them if n >= T)."""
+    if n >= T:
+        return torch.arange(T, dtype=torch.int64)
+    g = generator(seed, "sample", "cpu")
+    return torch.randperm(T, generator=g)[:n].sort().values
+
+
+# The named workloads: (shape, T, hot experts).
+WORKLOADS = {
+    "tiny": (TINY, 128, 0),
+    "decode": (BEAM, 16, 0),
+    "prefill": (BEAM, 4096, 0),
+    "skewed": (BEAM, 32768, 16),
+}
+SWEEP_T = (1, 8, 64, 256, 1024, 4096, 16384)

@@ -1,0 +1,248 @@
+"""Checks that pin the CPU oracle to facts fixed outside itself.
+
+Each check takes a loaded oracle build and raises AssertionError when the oracle breaks
+the fact it pins. The same checks run against the real oracle (tests/test_oracle_pins.py)
+and against copies of it with planted mistakes (tests/test_oracle_mutants.py), which must
+each fail at least one check.
+
+What pins what:
+  * hand-worked routing cases (tests/golden/routing_handworked.json): group rule,
+    masking of dropped groups, tie order, bias for selection only, weights;
+  * brute force over all C(n_group, topk_group) group subsets and all top_k subsets of
+    the candidates (small configs): the selection maximises the ranked sums;
+  * reductions to library routines: torch.topk for group top-2 sums and for the plain
+    top-k case; scipy's expit for the sigmoid; numpy FP64 matmul for the logits;
+    torch float64 matmuls + torch.nn.functional.silu for the SwiGLU experts;
+  * invariants: distinct experts inside kept groups, weights > 0 summing to the scale;
+  * closed forms: all-zero input -> experts 0..7, weights scale/8, output 0; identical
+    experts -> output = scale * expert(x).
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import scipy.special
+import torch
+
+from sparse_moe_transformer_bias_b300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "routing_handworked.json")
+
+
+def small_shape(**kw):
+    base = dict(d=48, I=40, E=16, n_group=4, topk_group=2, top_k=3, scale=2.5)
+    base.update(kw)
+    return W.MoEShape(**base)
+
+
+def random_routing_inputs(shape, T, seed=0, logit_std=1.0):
+    rng = np.random.default_rng(seed)
+    logits = (rng.standard_normal((T, shape.E)) * logit_std).astype(np.float32)
+    bias = rng.uniform(-0.1, 0.1, shape.E).astype(np.float32)
+    return logits, bias
+
+
+def tiny_layer(seed=0, T=24, shape=W.TINY):
+    x = W.make_tokens(shape, T, seed)
+    wr, b = W.make_router(shape, seed)
+    wg, wu, wd = W.make_experts(shape, seed)
+    return x, wr, b, wg, wu, wd
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _torch_expert(x64, wg, wu, wd):
+    """SwiGLU expert with torch float64 ops: down(silu(gate x) * up x)."""
+    g = x64 @ wg.double().T
+    u = x64 @ wu.double().T
+    return (torch.nn.functional.silu(g) * u) @ wd.double().T
+
+
+# ----------------------------------------------------------------------------------------
+
+def check_golden_cases(orc):
+    spec = json.load(open(GOLDEN))
+    c = spec["config"]
+    shape = W.MoEShape(d=8, I=8, E=c["E"], n_group=c["n_group"], topk_group=c["topk_group"], top_k=c["top_k"],
+                       scale=c["scale"])
+    for case in spec["cases"]:
+        bias = np.full(shape.E, case["default_bias"], np.float32)
+        for e, v in case["bias"].items():
+            bias[int(e)] = v
+        for tok in case["tokens"]:
+            l = np.full((1, shape.E), tok["default_logit"], np.float32)
+            for e, v in tok["logits"].items():
+                l[0, int(e)] = v
+            idx, w, dbg = orc.route(shape, l, bias, debug=True)
+            assert list(dbg["groups"][0]) == tok["expect_groups"], (case["name"], dbg["groups"][0])
+            assert list(idx[0]) == tok["expect_idx"], (case["name"], idx[0])
+            np.testing.assert_allclose(w[0], tok["expect_w"], rtol=2e-6, err_msg=case["name"])
+
+
+def check_invariants(orc, shape=W.BEAM, T=3000, seed=1):
+    logits, bias = random_routing_inputs(shape, T, seed, logit_std=1.5)
+    idx, w, dbg = orc.route(shape, logits, bias, debug=True)
+    S = shape.E // shape.n_group
+    for t in range(T):
+        ids = idx[t]
+        assert len(set(ids.tolist())) == shape.top_k, ("duplicate expert", t, ids)
+        kept = set(dbg["groups"][t].tolist())
+        assert len(kept) == shape.topk_group
+        assert all((e // S) in kept for e in ids), ("expert outside kept groups", t)
+        # every picked score >= every unpicked candidate score of the kept groups
+        cand = [e for e in range(shape.E) if (e // S) in kept and e not in set(ids.tolist())]
+        cmin = min(dbg["c"][t, ids])
+        assert all(dbg["c"][t, e] <= cmin for e in cand), ("unpicked candidate beats a pick", t)
+        # descending slot order
+        cs = dbg["c"][t, ids]
+        assert np.all(cs[:-1] >= cs[1:]), ("slot order", t)
+    assert np.all(w > 0)
+    np.testing.assert_allclose(w.astype(np.float64).sum(1), shape.scale, rtol=2e-6)
+    np.testing.assert_allclose(dbg["w64"].sum(1), shape.scale, rtol=1e-12)
+
+
+def check_sigmoid_and_bias(orc, shape=W.BEAM, T=500, seed=2):
+    logits, bias = random_routing_inputs(shape, T, seed, logit_std=3.0)
+    _, _, dbg = orc.route(shape, logits, bias, debug=True)
+    ref = scipy.special.expit(logits.astype(np.float64)).astype(np.float32)
+    ulps = np.abs(dbg["s"].view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+    assert ulps.max() <= 1 and (ulps > 0).mean() < 1e-3, ("sigmoid", ulps.max(), (ulps > 0).mean())
+    # biased score: one FP32 add of the rounded sigmoid and the bias
+    np.testing.assert_array_equal(dbg["c"], (dbg["s"] + bias[None, :]).astype(np.float32))
+
+
+def check_group_scores_vs_topk(orc, shape=W.BEAM, T=500, seed=3):
+    logits, bias = random_routing_inputs(shape, T, seed)
+    _, _, dbg = orc.route(shape, logits, bias, debug=True)
+    c = torch.from_numpy(dbg["c"]).view(T, shape.n_group, shape.E // shape.n_group)
+    top2 = torch.topk(c, 2, dim=-1).values
+    ref = (top2[..., 0] + top2[..., 1]).numpy()
+    np.testing.assert_array_equal(dbg["gs"], ref)
+
+
+def check_group_choice_brute_force(orc, shape=W.BEAM, T=400, seed=4):
+    logits, bias = random_routing_inputs(shape, T, seed)
+    _, _, dbg = orc.route(shape, logits, bias, debug=True)
+    subsets = list(itertools.combinations(range(shape.n_group), shape.topk_group))
+    for t in range(T):
+        gs = dbg["gs"][t].astype(np.float64)
+        best = max(subsets, key=lambda sub: (sum(gs[g] for g in sub), [-g for g in sub]))
+        assert set(best) == set(dbg["groups"][t].tolist()), (t, best, dbg["groups"][t])
+
+
+def check_selection_brute_force_small(orc, T=300, seed=5):
+    """Small config: enumerate all group subsets, then all top_k subsets of the kept
+    candidates; the oracle's picks must be the best subset by (group score sum, then
+    biased score sum)."""
+    shape = small_shape()
+    logits, bias = random_routing_inputs(shape, T, seed)
+    idx, _, dbg = orc.route(shape, logits, bias, debug=True)
+    S = shape.E // shape.n_group
+    s64 = scipy.special.expit(logits.astype(np.float64)).astype(np.float32)
+    for t in range(T):
+        c = (s64[t] + bias).astype(np.float32).astype(np.float64)
+        gs = [sum(sorted(c[g * S:(g + 1) * S], reverse=True)[:2]) for g in range(shape.n_group)]
+        kept = max(itertools.combinations(range(shape.n_group), shape.topk_group), key=lambda sub: sum(gs[g] for g in sub))
+        cand = [e for e in range(shape.E) if e // S in kept]
+        picks = max(itertools.combinations(cand, shape.top_k), key=lambda sub: sum(c[e] for e in sub))
+        assert set(picks) == set(idx[t].tolist()), (t, picks, idx[t])
+
+
+def check_plain_topk_reduction(orc, T=300, seed=6):
+    """All groups kept and zero bias: routing is torch.topk of the logits (sigmoid is
+    monotone), also with a single group."""
+    for shape in (W.MoEShape(d=8, I=8, topk_group=8), W.MoEShape(d=8, I=8, n_group=1, topk_group=1)):
+        logits, _ = random_routing_inputs(shape, T, seed)
+        bias = np.zeros(shape.E, np.float32)
+        idx, _ = orc.route(shape, logits, bias)
+        ref = torch.topk(torch.from_numpy(logits), shape.top_k, dim=1).indices.numpy()
+        np.testing.assert_array_equal(idx, ref)
+
+
+def check_logits_vs_matmul(orc, seed=7):
+    shape = W.TINY
+    x = W.make_tokens(shape, 64, seed)
+    wr, _ = W.make_router(shape, seed)
+    l = orc.router_logits(shape, _bits(x), wr.numpy())
+    ref = (x.double().numpy() @ wr.double().numpy().T).astype(np.float32)
+    ulps = np.abs(l.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+    assert ulps.max() <= 1, ulps.max()
+
+
+def check_expert_vs_torch(orc, seed=8):
+    shape = W.TINY
+    x, _, _, wg, wu, wd = tiny_layer(seed, T=4)
+    for t, e in ((0, 3), (1, 200), (3, 77)):
+        y = orc.expert(shape, x[t].double().numpy(), _bits(wg[e]), _bits(wu[e]), _bits(wd[e]))
+        ref = _torch_expert(x[t:t + 1].double(), wg[e], wu[e], wd[e])[0].numpy()
+        np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
+
+
+def check_forward_combination(orc, seed=9):
+    """Forward = sum_k w_k * expert_{e_k}(x), with the weights re-derived from scipy's
+    sigmoid of the logits and the experts from torch float64 ops."""
+    shape = W.TINY
+    x, wr, b, wg, wu, wd = tiny_layer(seed, T=12)
+    out, idx, w = orc.forward(shape, _bits(x), b.numpy(), lambda e: (_bits(wg[e]), _bits(wu[e]), _bits(wd[e])),
+                              router_w=wr.numpy())
+    logits = orc.router_logits(shape, _bits(x), wr.numpy())
+    s = scipy.special.expit(logits.astype(np.float64)).astype(np.float32).astype(np.float64)
+    for t in range(x.shape[0]):
+        ws = s[t, idx[t]]
+        ws = shape.scale * ws / ws.sum()
+        np.testing.assert_allclose(w[t], ws, rtol=2e-6)
+        ref = sum(ws[k] * _torch_expert(x[t:t + 1].double(), wg[idx[t, k]], wu[idx[t, k]], wd[idx[t, k]])[0]
+                  for k in range(shape.top_k)).numpy()
+        np.testing.assert_allclose(out[t], ref, rtol=1e-9, atol=1e-12)
+
+
+def check_zero_input(orc, seed=10):
+    shape = W.TINY
+    _, wr, _, wg, wu, wd = tiny_layer(seed, T=1)
+    x = torch.zeros((3, shape.d), dtype=torch.bfloat16)
+    b = np.full(shape.E, 0.037, np.float32)
+    out, idx, w = orc.forward(shape, _bits(x), b, lambda e: (_bits(wg[e]), _bits(wu[e]), _bits(wd[e])),
+                              router_w=wr.numpy())
+    assert (idx == np.arange(8)[None, :]).all(), idx
+    assert (w == np.float32(shape.scale / 8)).all(), w
+    assert (out == 0).all()
+
+
+def check_identical_experts(orc, seed=11):
+    shape = W.TINY
+    x, wr, b, wg, wu, wd = tiny_layer(seed, T=6)
+    one = (_bits(wg[5]), _bits(wu[5]), _bits(wd[5]))
+    out, _, _ = orc.forward(shape, _bits(x), b.numpy(), lambda e: one, router_w=wr.numpy())
+    ref = shape.scale * _torch_expert(x.double(), wg[5], wu[5], wd[5]).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-12)
+
+
+def check_given_selection(orc, seed=12):
+    """With the selection handed in, the oracle uses exactly those experts and re-derives
+    their weights from its own sigmoid scores."""
+    shape = W.TINY
+    x, wr, b, wg, wu, wd = tiny_layer(seed, T=3)
+    experts = lambda e: (_bits(wg[e]), _bits(wu[e]), _bits(wd[e]))
+    pick = np.array([[7, 6, 5, 4, 3, 2, 1, 0], [255, 0, 128, 64, 32, 16, 8, 4], [10, 11, 12, 13, 14, 15, 16, 17]],
+                    np.int32)
+    out, idx, w = orc.forward(shape, _bits(x), b.numpy(), experts, router_w=wr.numpy(), idx_in=pick)
+    assert (idx == pick).all()
+    logits = orc.router_logits(shape, _bits(x), wr.numpy())
+    s = scipy.special.expit(logits.astype(np.float64)).astype(np.float32).astype(np.float64)
+    for t in range(3):
+        ws = shape.scale * s[t, pick[t]] / s[t, pick[t]].sum()
+        np.testing.assert_allclose(w[t], ws, rtol=2e-6)
+
+
+ALL_CHECKS = [
+    check_golden_cases, check_invariants, check_sigmoid_and_bias, check_group_scores_vs_topk,
+    check_group_choice_brute_force, check_selection_brute_force_small, check_plain_topk_reduction,
+    check_logits_vs_matmul, check_expert_vs_torch, check_forward_combination, check_zero_input,
+    check_identical_experts, check_given_selection,
+]

@@ -1,0 +1,45 @@
+"""The pins are strong enough: each plausible mistake planted in a copy of the oracle
+(on the CPU) must make at least one pin fail. The real oracle is never modified."""
+import pytest
+
+import pins
+from oracle import oracle as O
+
+# (name, text in the oracle source, replacement). Each text occurs exactly once, and every
+# mutant keeps all array accesses in bounds.
+MUTANTS = [
+    ("sigmoid_sign", "exp(-(double)l[e])", "exp((double)l[e])"),
+    ("bias_dropped", "c[e] = s[e] + bias[e];", "c[e] = s[e];"),
+    ("group_score_max_only", "scratch[0].key + scratch[1].key : scratch[0].key", "scratch[0].key : scratch[0].key"),
+    ("dropped_groups_scored_zero", "if (kept[e / S]) { scratch[n_cand].key = c[e];",
+     "{ scratch[n_cand].key = kept[e / S] ? c[e] : 0.0f;"),
+    ("ties_to_higher_index", "return (a->id > b->id) - (a->id < b->id);", "return (a->id < b->id) - (a->id > b->id);"),
+    ("ascending_rank", "if (a->key > b->key) return -1;", "if (a->key < b->key) return -1;"),
+    ("weights_from_biased_score", "double wk = cf->scale * (double)s[idx[k]] / sum;",
+     "double wk = cf->scale * (double)c[idx[k]] / sum;"),
+    ("scale_missing", "double wk = cf->scale * (double)s[idx[k]] / sum;", "double wk = (double)s[idx[k]] / sum;"),
+    ("one_group_short", "for (int r = 0; r < cf->topk_group; r++) {", "for (int r = 0; r + 1 < cf->topk_group; r++) {"),
+    ("gate_transposed", "x[j] * bf16_value(wg[(int64_t)i * d + j]);", "x[j] * bf16_value(wg[(int64_t)j * I + i]);"),
+    ("down_transposed", "h[i] * bf16_value(wd[(int64_t)j * I + i]);", "h[i] * bf16_value(wd[(int64_t)i * d + j]);"),
+    ("sigmoid_not_silu", "h[i] = g / (1.0 + exp(-g)) * u;", "h[i] = 1.0 / (1.0 + exp(-g)) * u;"),
+    ("silu_on_up", "h[i] = g / (1.0 + exp(-g)) * u;", "h[i] = u / (1.0 + exp(-u)) * g;"),
+    ("combine_drops_slot", "for (int k = 0; k < K; k++) acc += w64", "for (int k = 0; k + 1 < K; k++) acc += w64"),
+    ("logits_transposed", "(double)wr[(int64_t)e * c->d + j]", "(double)wr[(int64_t)j * c->E + e]"),
+    ("logits_kept_fp64_sigmoid_in_fp32", "s[e] = (float)(1.0 / (1.0 + exp(-(double)l[e])));",
+     "s[e] = 1.0f / (1.0f + (float)exp(-(double)l[e]) * 1.0000005f);"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new):
+    src = open(O.SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} must occur once"
+    orc = O.Oracle(O.build_variant(src.replace(old, new), name))
+    caught = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except (AssertionError, RuntimeError) as exc:  # noqa: PERF203
+            caught.append((check.__name__, type(exc).__name__))
+            break
+    assert caught, f"no pin catches the planted mistake {name}"
