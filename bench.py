@@ -1,0 +1,391 @@
+"""Benchmark of the Beam routed-MoE forward pass (libbeam_moe.so) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|tiny|T<n>]
+                    [--impl reference] [--no-secondary]
+
+A step is one beam_moe_forward call over one batch of T tokens: router, dispatch,
+gate/up GEMM with SwiGLU, down GEMM, combine. Inputs and weights are synthetic, seeded,
+of Beam's layer shape, resident in HBM before timing starts. L2 is flushed (a 512 MB
+write) before every timed step; each step is bracketed by CUDA events on the launching
+stream and the reported time is the sum over K steps. Under torchrun each rank runs an
+independent replica on its own GPU (the path does not shard across GPUs here), and the
+time is the max over ranks.
+
+The default workload is Beam decode (T=16); one JSON line is printed by rank 0, carrying
+the dominant kernel's roofline, the CPU oracle's throughput on a bounded sample, the
+end-to-end number through host buffers, and a secondary prefill (T=4096) measurement.
+--impl reference times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sparse_moe_transformer_bias_b300 import abi, moe, workloads as W  # noqa: E402
+
+METRIC = "Beam MoE-layer tokens/s (T=16 decode, T=4096 prefill); % of roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM bytes (read + write) per launch of the dominant kernel from ncu captures; None when
+# the kernel changed after the capture. Keys: workload name.
+TRAFFIC = {}
+
+
+def peaks():
+    try:
+        p = json.load(open(PEAKS_FILE))
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload(name, n_group=8):
+    if name in W.WORKLOADS:
+        shape, T, hot = W.WORKLOADS[name]
+    elif name.startswith("T") and name[1:].isdigit():
+        shape, T, hot = W.BEAM, int(name[1:]), 0
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    if n_group != shape.n_group:
+        # Fewer expert groups (32 experts each): a smaller device footprint of the same
+        # kernels, used for profiler captures.
+        shape = W.MoEShape(d=shape.d, I=shape.I, E=32 * n_group, n_group=n_group,
+                           topk_group=min(shape.topk_group, n_group), top_k=shape.top_k, scale=shape.scale)
+        name = f"{name}_E{shape.E}"
+    return name, shape, T, hot
+
+
+# ---------------------------------------------------------------- clocks sampler
+class Clocks:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the measured arm
+def make_layer(shape, T, hot, device, experts=None, seed=0):
+    x = W.make_tokens(shape, T, seed, device)
+    wr, b = W.make_router(shape, seed, device, hot_experts=hot)
+    if experts is None:
+        experts = W.make_experts(shape, seed, device)
+    return x, wr, b, experts
+
+
+def algorithmic(shape, T, n_touched, rows):
+    """Algorithmic FLOPs and bytes of the whole layer and of each GEMM (one launch each)."""
+    d, I, E, K = shape.d, shape.I, shape.E, shape.top_k
+    layer_flops = T * (K * 3 * 2 * d * I + 2 * d * E)
+    layer_bytes = n_touched * 3 * d * I * 2 + E * d * 4 + E * 4 + 2 * T * d * 2 + T * K * 8
+    gateup = {"flops": 2 * rows * d * I * 2, "bytes": n_touched * 2 * I * d * 2 + rows * d * 2 + rows * I * 2}
+    down = {"flops": 2 * rows * I * d, "bytes": n_touched * d * I * 2 + rows * I * 2 + rows * d * 4}
+    return layer_flops, layer_bytes, {"gateup_gemm": gateup, "down_gemm": down}
+
+
+def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=True):
+    x, wr, b, (wg, wu, wd) = make_layer(shape, T, hot, device, experts)
+    out = torch.empty((T, shape.d), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream()
+    idx, _ = moe.route(x, wr, b, shape)
+    n_touched = int(torch.unique(idx).numel())
+    rows = T * shape.top_k
+
+    def step():
+        moe.forward(x, wr, b, wg, wu, wd, shape, out=out, stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    launches = abi.beam_moe_last_launch_count()
+
+    # Pass 1: the headline, no stage events inside the step.
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    clocks = Clocks(torch.cuda.current_device())
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(steps):
+        flush.zero_()
+        e0[i].record(stream)
+        step()
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    step_ms = [a.elapsed_time(c) for a, c in zip(e0, e1)]
+    total_ms = max_over_ranks(sum(step_ms))
+
+    # Pass 2: per-stage durations from the library's own events on the same stream.
+    abi.beam_moe_timing_enable(True)
+    stage_sum = {s: 0.0 for s in abi.STAGES}
+    n2 = max(3, min(steps, 50))
+    for _ in range(n2):
+        flush.zero_()
+        step()
+        for k, v in abi.beam_moe_timing_read().items():
+            stage_sum[k] += v
+    abi.beam_moe_timing_enable(False)
+    stage_ms = {k: v / n2 for k, v in stage_sum.items()}
+
+    layer_flops, layer_bytes, kern = algorithmic(shape, T, n_touched, rows)
+    t_roof_s = max(layer_flops / (pk["bf16_tflops"] * 1e12), layer_bytes / (pk["hbm_gbs"] * 1e9))
+    ms_per_step = total_ms / steps
+    dom = max(("gateup_gemm", "down_gemm"), key=lambda k: stage_ms[k])
+    kf, kb = kern[dom]["flops"], kern[dom]["bytes"]
+    t_dom = stage_ms[dom] * 1e-3
+    hbm_bound = kb / (pk["hbm_gbs"] * 1e9) >= kf / (pk["bf16_tflops"] * 1e12)
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": kb / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": kf / t_dom / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
+    roof["kernel_ms"] = stage_ms[dom]
+    tr = TRAFFIC.get(name)
+    roof["traffic"] = tr["bytes"] if tr and tr.get("kernel") == dom else None
+
+    res = {
+        "value": T * steps / (total_ms * 1e-3),
+        "ms_per_step": ms_per_step,
+        "roofline": roof,
+        "layer_roofline": {"t_roof_ms": t_roof_s * 1e3, "frac": t_roof_s * 1e3 / ms_per_step,
+                           "flops": layer_flops, "bytes": layer_bytes,
+                           "tensor_frac_of_burst": layer_flops / (pk["bf16_tflops"] * 1e12) / (ms_per_step * 1e-3)},
+        "stage_ms": stage_ms,
+        "n_touched_experts": n_touched,
+        "gpu_launches": launches * steps,
+        "clocks": clk,
+    }
+    if e2e:
+        res["e2e"] = measure_e2e(shape, T, x, wr, b, wg, wu, wd, steps, warmup, flush)
+    return res
+
+
+def measure_e2e(shape, T, x, wr, b, wg, wu, wd, steps, warmup, flush):
+    """Host tokens in, host output out, through the public call (moe.forward_host): the
+    H2D copy of the step's tokens, the forward pass and the D2H copy of its output are all
+    inside the timed region."""
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty((T, shape.d), dtype=torch.bfloat16, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    out_dev = torch.empty((T, shape.d), dtype=torch.bfloat16, device=x.device)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        moe.forward_host(x_host, wr, b, wg, wu, wd, shape, x_dev=x_dev, out_dev=out_dev, out_host=out_host,
+                         stream=stream)
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        moe.forward_host(x_host, wr, b, wg, wu, wd, shape, x_dev=x_dev, out_dev=out_dev, out_host=out_host,
+                         stream=stream)
+        total += time.perf_counter() - t0
+    total = max_over_ranks(total * 1e3) * 1e-3
+    return {"value": T * steps / total, "unit": "tokens/s", "h2d_bytes_per_step": T * shape.d * 2,
+            "d2h_bytes_per_step": T * shape.d * 2, "timer": "host wall clock around each synchronous step"}
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+def oracle_tokens_per_s(shape, x, wr, b, wg, wu, wd, n_tokens, seed=0):
+    """The CPU oracle (as it stands) on a seeded sample of tokens of the workload: router
+    logits, routing, experts, combine. Returns (tokens/s, seconds, sample, threads)."""
+    from oracle import oracle as O
+    T = x.shape[0]
+    tokens = W.sample_tokens(T, n_tokens, seed=seed).numpy()
+    xb = O.bf16_bits(x)
+    wr_h = wr.cpu().numpy()
+    b_h = b.cpu().numpy()
+    logits = O.router_logits(shape, xb[tokens], wr_h)
+    idx, _ = O.route(shape, logits, b_h)
+    needed = set(np.unique(idx).tolist())
+    experts = O.experts_from(wg, wu, wd, only=needed)
+    host = {e: experts(e) for e in needed}
+    t0 = time.perf_counter()
+    O.forward(shape, xb, b_h, lambda e: host.get(e), tokens=tokens, router_w=wr_h)
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    return len(tokens) / dt, dt, f"{len(tokens)} of {T} tokens (seeded), full layer incl. router", threads
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def rank_world():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v):
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([float(v)], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return float(v)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-tokens", type=int, default=None)
+    ap.add_argument("--n-group", type=int, default=8, help="expert groups of 32 (8 = Beam); fewer for profiling")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, world, local = rank_world()
+    name, shape, T, hot = workload(args.workload, args.n_group)
+    pk, pk_src = peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        torch.cuda.set_device(local)
+        x, wr, b, (wg, wu, wd) = make_layer(shape, T, hot, "cuda")
+        n_tok = args.oracle_tokens or (4 if shape.d >= 1024 else 64)
+        vals, secs = [], 0.0
+        for i in range(args.warmup + args.steps):
+            v, dt, sample, thr = oracle_tokens_per_s(shape, x, wr, b, wg, wu, wd, min(n_tok, T), seed=100 + i)
+            if i >= args.warmup:
+                vals.append(dt)
+                secs += dt
+        tokens = min(n_tok, T) * args.steps
+        value = tokens / secs
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"{name} T={T}", "d": shape.d, "I": shape.I, "E": shape.E},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                             "sample": f"{min(n_tok, T)} seeded tokens of {T} per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = "cuda"
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    experts = W.make_experts(shape, 0, device)
+    torch.cuda.synchronize()
+
+    res = measure(name, shape, T, hot, args.steps, args.warmup, experts, device, flush, pk)
+    secondary = None
+    if not args.no_secondary and name == "decode" and args.n_group == 8:
+        s_name, s_shape, s_T, s_hot = workload("prefill")
+        s_steps = max(10, min(args.steps, 50))
+        sec = measure(s_name, s_shape, s_T, s_hot, s_steps, args.warmup, experts, device, flush, pk, e2e=False)
+        secondary = {"workload": f"Beam prefill T={s_T}", "value": sec["value"], "unit": "tokens/s",
+                     "ms_per_step": sec["ms_per_step"], "steps": s_steps, "roofline": sec["roofline"],
+                     "layer_roofline": sec["layer_roofline"], "stage_ms": sec["stage_ms"],
+                     "n_touched_experts": sec["n_touched_experts"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x, wr, b, (wg, wu, wd) = make_layer(shape, T, hot, device, experts)
+        n_tok = args.oracle_tokens or min(T, 16)
+        v, dt, sample, thr = oracle_tokens_per_s(shape, x, wr, b, wg, wu, wd, n_tok)
+        cpu = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle", "sample": sample, "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": res["value"] * world, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) FP32 router, U(-0.1,0.1) bias, "
+                    "BF16 experts std 1/sqrt(fan_in))",
+            "config": {"workload": f"Beam MoE layer {name} T={T}" + (f", {hot} hot experts" if hot else ""),
+                       "T": T, "d": shape.d, "I": shape.I, "E": shape.E, "n_group": shape.n_group,
+                       "topk_group": shape.topk_group, "top_k": shape.top_k, "scale": shape.scale,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed (512 MB write) before every timed step"},
+            "roofline": {**res["roofline"], "peak_source": pk_src + " (MEASURED_PEAKS.json burst)"
+                         if pk_src == "measured" else "fallback"},
+            "layer_roofline": res["layer_roofline"],
+            "stage_ms": res["stage_ms"],
+            "n_touched_experts": res["n_touched_experts"],
+            "cpu_baseline": cpu,
+            "e2e": res["e2e"],
+            "gpu_launches": res["gpu_launches"],
+            "clocks": res["clocks"],
+        }
+        if secondary:
+            line["secondary"] = secondary
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,142 @@
+/*
+ * beam_moe.h - C ABI of the B300 (sm_103a) routed-MoE forward library, libbeam_moe.so.
+ *
+ * The operation is the forward pass of one routed Mixture-of-Experts block of Reflection's
+ * Beam model, as the release pages describe it:
+ *   - "Reflection releases Beam, a 501B open MoE model with 1M context" (Glonce),
+ *     Architecture paragraph: 256 experts scored with a sigmoid, split into 8 groups of 32;
+ *     the 4 best groups are kept and the top 8 experts picked from them; no shared expert;
+ *     expert outputs combined with normalized router weights and scaled by 2.5; each
+ *     expert a SwiGLU MLP with intermediate size 2,560 on hidden size 5,120.
+ *   - transformers "Beam" model doc, Overview, "Sparse MoE" bullet: a learned per-expert
+ *     bias balances load (selection); best topk_group of n_group groups; weights
+ *     normalized; output scaled by routed_scaling_factor.
+ *   - same page, paragraph after the bullets: routing and the SwiGLU activation run in
+ *     FP32; router weights and expert bias are FP32; returned router logits are FP32.
+ * Readings where the pages are silent: a group scores the sum of its two largest biased
+ * scores (the DeepSeek-V3 convention the pages name); the bias is used for selection only;
+ * ties go to the lower group, then the lower expert index; experts of dropped groups are
+ * excluded; slots are ordered by descending biased score; the scale is folded into the
+ * weights (they sum to `scale`); experts have no linear biases.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers on the current CUDA device, row-major and contiguous,
+ *     16-byte aligned. The caller owns every buffer; the library keeps no pointer after
+ *     a call returns. Outputs must not alias inputs.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream): results are valid
+ *     once the stream has synchronised. No entry point synchronises the host except
+ *     beam_moe_device_status and beam_moe_timing_read.
+ *   - Scratch memory is taken from a library-owned stream-ordered pool on the current
+ *     device and returned before the call's work completes (cudaMallocFromPoolAsync /
+ *     cudaFreeAsync on `stream`); the pool keeps freed memory cached for the next call.
+ *   - Return value: BEAM_MOE_OK (0) or a negative code; beam_moe_last_error() returns a
+ *     message for the calling thread's last failure. T == 0 returns BEAM_MOE_OK and
+ *     launches nothing. Device kernels never trap: a kernel that detects a bad index or a
+ *     wait that ran past its limit records a code that beam_moe_device_status() returns.
+ *   - Results are deterministic run to run for identical inputs.
+ *   - Inputs must be finite.
+ *
+ * Supported shapes: d and I multiples of 128; E = 32 * n_group with 1 <= n_group <= 8;
+ * 1 <= topk_group <= n_group; 1 <= top_k <= min(32, 32 * topk_group);
+ * 0 <= T <= BEAM_MOE_MAX_TOKENS.
+ */
+#ifndef BEAM_MOE_H
+#define BEAM_MOE_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+#include <cuda_bf16.h>
+
+#if defined(__GNUC__)
+#define BEAM_MOE_API __attribute__((visibility("default")))
+#else
+#define BEAM_MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BEAM_MOE_OK 0
+#define BEAM_MOE_ERR_ARG (-1)        /* null pointer, negative T, T too large, bad config */
+#define BEAM_MOE_ERR_ALIGN (-2)      /* a pointer is not 16-byte aligned */
+#define BEAM_MOE_ERR_CUDA (-3)       /* a CUDA runtime/driver call failed (message says which) */
+#define BEAM_MOE_ERR_DEVICE (-4)     /* a kernel recorded a device-side error (beam_moe_device_status) */
+
+#define BEAM_MOE_MAX_TOKENS 262144
+
+/* Layer shape. Field names d, I, E are ours; n_group, topk_group and scale
+ * (routed_scaling_factor) follow the transformers BeamConfig. */
+typedef struct {
+    int d;            /* hidden size (Beam: 5120) */
+    int I;            /* expert intermediate size (Beam: 2560) */
+    int E;            /* routed experts (Beam: 256) */
+    int n_group;      /* expert groups (Beam: 8) */
+    int topk_group;   /* groups kept per token (Beam: 4) */
+    int top_k;        /* experts per token (Beam: 8) */
+    float scale;      /* routed_scaling_factor (Beam: 2.5) */
+} beam_moe_config;
+
+/* Beam's layer: d=5120, I=2560, E=256, n_group=8, topk_group=4, top_k=8, scale=2.5. */
+BEAM_MOE_API beam_moe_config beam_moe_default_config(void);
+
+/* Router: FP32 logits l = x . router_w^T, s = sigmoid(l), c = s + expert_bias (selection
+ * only), group score = top-2 sum of c, keep topk_group groups, pick top_k experts among
+ * them by c, weights w_k = scale * s_k / sum_k s_k.
+ *   x            bf16 [T, d]
+ *   router_w     fp32 [E, d]
+ *   expert_bias  fp32 [E]
+ *   topk_idx     int32 [T, top_k]  out: expert ids, descending c, ties -> lower id
+ *   topk_w       fp32  [T, top_k]  out: weights, sum = scale per token
+ * beam_moe_route uses Beam's shape (beam_moe_default_config()). */
+BEAM_MOE_API int beam_moe_route(const __nv_bfloat16 *x, const float *router_w, const float *expert_bias, int T,
+                   int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+BEAM_MOE_API int beam_moe_route_ex(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
+                      const float *expert_bias, int T, int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+
+/* Whole MoE block: route as above, then out[t] = sum_k w_k * SwiGLU_{e_k}(x[t]) with
+ * SwiGLU_e(v) = w_down[e] . ( silu(w_gate[e] . v) * (w_up[e] . v) ), silu(z) = z sigmoid(z).
+ *   w_gate, w_up  bf16 [E, I, d]   (nn.Linear [out, in] per expert)
+ *   w_down        bf16 [E, d, I]
+ *   out           bf16 [T, d]
+ * Numerics: FP32 router; BF16 tensor-core products with FP32 accumulation; SwiGLU in FP32,
+ * its result rounded to BF16 for the down product; FP32 down outputs combined in FP32 in
+ * slot order, rounded once to BF16.
+ * beam_moe_forward uses Beam's shape. */
+BEAM_MOE_API int beam_moe_forward(const __nv_bfloat16 *x, const float *router_w, const float *expert_bias,
+                     const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up, const __nv_bfloat16 *w_down, int T,
+                     __nv_bfloat16 *out, cudaStream_t stream);
+BEAM_MOE_API int beam_moe_forward_ex(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
+                        const float *expert_bias, const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up,
+                        const __nv_bfloat16 *w_down, int T, __nv_bfloat16 *out, cudaStream_t stream);
+
+/* Router logits only (output_router_logits in the transformers doc, Notes): the same
+ * kernels as the router's first stage; logits fp32 [T, E]. */
+BEAM_MOE_API int beam_moe_router_logits(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w, int T,
+                           float *logits, cudaStream_t stream);
+
+/* Message for the calling thread's last non-zero return (empty string if none). */
+BEAM_MOE_API const char *beam_moe_last_error(void);
+
+/* Synchronises `stream`, then returns and clears the current device's kernel status word:
+ * 0 if no kernel recorded an error since the last call, else BEAM_MOE_ERR_DEVICE (the
+ * message names the recorded code: 1 = an expert index out of range reached dispatch,
+ * 2 = a pipeline wait in a GEMM ran past its limit). */
+BEAM_MOE_API int beam_moe_device_status(cudaStream_t stream);
+
+/* Per-stage timing for profiling. While enabled (per thread), each forward/route call
+ * records CUDA events on its stream around each stage; beam_moe_timing_read synchronises
+ * on the last call's final event and writes up to max_stages durations in milliseconds
+ * (stage order: router logits, router select, dispatch count, dispatch scan, dispatch
+ * scatter, gather, gate/up GEMM, down GEMM, combine; unrun stages read 0). Returns the
+ * number of stages, or a negative error. */
+BEAM_MOE_API int beam_moe_timing_enable(int enable);
+BEAM_MOE_API int beam_moe_timing_read(float *ms, int max_stages);
+
+/* Number of kernel launches the last forward/route call on this thread made. */
+BEAM_MOE_API int beam_moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BEAM_MOE_H */

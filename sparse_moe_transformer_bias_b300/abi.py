@@ -1,0 +1,164 @@
+"""Thin ctypes binding of libbeam_moe.so (include/beam_moe.h): same names, argument
+marshalling only. Every step of the MoE forward pass runs in the library's CUDA kernels;
+this module only turns torch tensors into device pointers and status codes into
+exceptions. There is no fallback: if the library is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libbeam_moe.so")
+
+BEAM_MOE_OK = 0
+BEAM_MOE_ERR_ARG = -1
+BEAM_MOE_ERR_ALIGN = -2
+BEAM_MOE_ERR_CUDA = -3
+BEAM_MOE_ERR_DEVICE = -4
+BEAM_MOE_MAX_TOKENS = 262144
+
+STAGES = ("router_logits", "router_select", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather",
+          "gateup_gemm", "down_gemm", "combine")
+
+# Every symbol include/beam_moe.h declares.
+EXPORTS = ("beam_moe_default_config", "beam_moe_route", "beam_moe_route_ex", "beam_moe_forward",
+           "beam_moe_forward_ex", "beam_moe_router_logits", "beam_moe_last_error", "beam_moe_device_status",
+           "beam_moe_timing_enable", "beam_moe_timing_read", "beam_moe_last_launch_count")
+
+
+class BeamMoeConfig(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int), ("n_group", ctypes.c_int),
+                ("topk_group", ctypes.c_int), ("top_k", ctypes.c_int), ("scale", ctypes.c_float)]
+
+    @classmethod
+    def of(cls, shape) -> "BeamMoeConfig":
+        return cls(shape.d, shape.I, shape.E, shape.n_group, shape.topk_group, shape.top_k, float(shape.scale))
+
+
+class BeamMoeError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"beam_moe error {code}: {message}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libbeam_moe.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with python -m sparse_moe_transformer_bias_b300.build")
+            L = ctypes.CDLL(LIB_PATH)
+            P = ctypes.c_void_p
+            i = ctypes.c_int
+            cfgp = ctypes.POINTER(BeamMoeConfig)
+            L.beam_moe_default_config.restype = BeamMoeConfig
+            L.beam_moe_default_config.argtypes = []
+            L.beam_moe_route.argtypes = [P, P, P, i, P, P, P]
+            L.beam_moe_route_ex.argtypes = [cfgp, P, P, P, i, P, P, P]
+            L.beam_moe_forward.argtypes = [P, P, P, P, P, P, i, P, P]
+            L.beam_moe_forward_ex.argtypes = [cfgp, P, P, P, P, P, P, i, P, P]
+            L.beam_moe_router_logits.argtypes = [cfgp, P, P, i, P, P]
+            L.beam_moe_last_error.restype = ctypes.c_char_p
+            L.beam_moe_last_error.argtypes = []
+            L.beam_moe_device_status.argtypes = [P]
+            L.beam_moe_timing_enable.argtypes = [i]
+            L.beam_moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), i]
+            L.beam_moe_last_launch_count.argtypes = []
+            for f in ("beam_moe_route", "beam_moe_route_ex", "beam_moe_forward", "beam_moe_forward_ex",
+                      "beam_moe_router_logits", "beam_moe_device_status", "beam_moe_timing_enable",
+                      "beam_moe_timing_read", "beam_moe_last_launch_count"):
+                getattr(L, f).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    """Device pointer of a tensor (None/0 passes a null pointer, an int passes through)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int):
+    if rc != BEAM_MOE_OK:
+        raise BeamMoeError(rc, load().beam_moe_last_error().decode())
+    return rc
+
+
+def _cfg(cfg):
+    if cfg is None:
+        return None
+    return ctypes.byref(cfg if isinstance(cfg, BeamMoeConfig) else BeamMoeConfig.of(cfg))
+
+
+def beam_moe_default_config() -> BeamMoeConfig:
+    return load().beam_moe_default_config()
+
+
+def beam_moe_route(x, router_w, expert_bias, T, topk_idx, topk_w, stream=None):
+    return _check(load().beam_moe_route(_ptr(x), _ptr(router_w), _ptr(expert_bias), int(T), _ptr(topk_idx),
+                                        _ptr(topk_w), _stream(stream)))
+
+
+def beam_moe_route_ex(cfg, x, router_w, expert_bias, T, topk_idx, topk_w, stream=None):
+    return _check(load().beam_moe_route_ex(_cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), int(T),
+                                           _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
+def beam_moe_forward(x, router_w, expert_bias, w_gate, w_up, w_down, T, out, stream=None):
+    return _check(load().beam_moe_forward(_ptr(x), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate), _ptr(w_up),
+                                          _ptr(w_down), int(T), _ptr(out), _stream(stream)))
+
+
+def beam_moe_forward_ex(cfg, x, router_w, expert_bias, w_gate, w_up, w_down, T, out, stream=None):
+    return _check(load().beam_moe_forward_ex(_cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate),
+                                             _ptr(w_up), _ptr(w_down), int(T), _ptr(out), _stream(stream)))
+
+
+def beam_moe_router_logits(cfg, x, router_w, T, logits, stream=None):
+    return _check(load().beam_moe_router_logits(_cfg(cfg), _ptr(x), _ptr(router_w), int(T), _ptr(logits),
+                                                _stream(stream)))
+
+
+def beam_moe_last_error() -> str:
+    return load().beam_moe_last_error().decode()
+
+
+def beam_moe_device_status(stream=None):
+    return _check(load().beam_moe_device_status(_stream(stream)))
+
+
+def beam_moe_timing_enable(enable: bool):
+    return _check(load().beam_moe_timing_enable(1 if enable else 0))
+
+
+def beam_moe_timing_read() -> dict:
+    buf = (ctypes.c_float * len(STAGES))()
+    n = load().beam_moe_timing_read(buf, len(STAGES))
+    if n < 0:
+        _check(n)
+    return {name: float(buf[i]) for i, name in enumerate(STAGES)}
+
+
+def beam_moe_last_launch_count() -> int:
+    return int(load().beam_moe_last_launch_count())

@@ -1,0 +1,363 @@
+// C ABI of libbeam_moe.so (declared and documented in include/beam_moe.h): argument
+// checks, per-device state (scratch pool, status word), scratch layout and the launch
+// sequence of the Beam MoE forward pass.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "beam_moe.h"
+#include "internal.cuh"
+
+namespace beam {
+namespace {
+
+thread_local char g_err[512] = "";
+thread_local int g_launches = 0;
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+// ---------------------------------------------------------------- per-device state
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    cudaMemPool_t pool = nullptr;
+    int* status = nullptr;  // device word written by kernels
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_state(DeviceState** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(BEAM_MOE_ERR_ARG, "device %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        if ((e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail(BEAM_MOE_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        cudaMemPoolProps props;
+        memset(&props, 0, sizeof props);
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if ((e = cudaMemPoolCreate(&s.pool, &props)) != cudaSuccess)
+            return fail(BEAM_MOE_ERR_CUDA, "cudaMemPoolCreate: %s", cudaGetErrorString(e));
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if ((e = cudaMalloc(&s.status, 16)) != cudaSuccess)
+            return fail(BEAM_MOE_ERR_CUDA, "cudaMalloc(status): %s", cudaGetErrorString(e));
+        if ((e = cudaMemset(s.status, 0, 16)) != cudaSuccess)
+            return fail(BEAM_MOE_ERR_CUDA, "cudaMemset(status): %s", cudaGetErrorString(e));
+        s.ready = true;
+    }
+    *out = &s;
+    return BEAM_MOE_OK;
+}
+
+int check_stream(cudaStream_t st) {
+    if (st == nullptr) return BEAM_MOE_OK;
+    int sdev = -1, cdev = -1;
+    if (cudaStreamGetDevice(st, &sdev) != cudaSuccess || cudaGetDevice(&cdev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(BEAM_MOE_ERR_ARG, "invalid stream");
+    }
+    if (sdev != cdev) return fail(BEAM_MOE_ERR_ARG, "stream belongs to device %d but device %d is current", sdev, cdev);
+    return BEAM_MOE_OK;
+}
+
+// ---------------------------------------------------------------- stage timing
+enum Stage { kLogits, kSelect, kCount, kScan, kScatter, kGather, kGateUp, kDown, kCombine, kNumStages };
+struct Timing {
+    bool enabled = false;
+    bool created = false;
+    int device = -1;
+    cudaEvent_t start[kNumStages], stop[kNumStages];
+    bool ran[kNumStages] = {};
+    cudaEvent_t last = nullptr;
+};
+thread_local Timing g_timing;
+
+void timing_begin_call() {
+    for (bool& r : g_timing.ran) r = false;
+    g_timing.last = nullptr;
+}
+void stage_begin(Stage s, cudaStream_t st) {
+    if (!g_timing.enabled) return;
+    cudaEventRecord(g_timing.start[s], st);
+}
+void stage_end(Stage s, cudaStream_t st) {
+    ++g_launches;
+    if (!g_timing.enabled) return;
+    cudaEventRecord(g_timing.stop[s], st);
+    g_timing.ran[s] = true;
+    g_timing.last = g_timing.stop[s];
+}
+
+// ---------------------------------------------------------------- checks and layout
+int check_cfg(const beam_moe_config* c) {
+    if (!c) return fail(BEAM_MOE_ERR_ARG, "config is null");
+    if (c->d < 128 || c->d % 128) return fail(BEAM_MOE_ERR_ARG, "d=%d must be a positive multiple of 128", c->d);
+    if (c->I < 128 || c->I % 128) return fail(BEAM_MOE_ERR_ARG, "I=%d must be a positive multiple of 128", c->I);
+    if (c->n_group < 1 || c->n_group > 8) return fail(BEAM_MOE_ERR_ARG, "n_group=%d must be in [1, 8]", c->n_group);
+    if (c->E != 32 * c->n_group) return fail(BEAM_MOE_ERR_ARG, "E=%d must equal 32 * n_group", c->E);
+    if (c->topk_group < 1 || c->topk_group > c->n_group)
+        return fail(BEAM_MOE_ERR_ARG, "topk_group=%d must be in [1, n_group]", c->topk_group);
+    if (c->top_k < 1 || c->top_k > 32 || c->top_k > 32 * c->topk_group)
+        return fail(BEAM_MOE_ERR_ARG, "top_k=%d must be in [1, min(32, 32 * topk_group)]", c->top_k);
+    if (!std::isfinite(c->scale)) return fail(BEAM_MOE_ERR_ARG, "scale must be finite");
+    return BEAM_MOE_OK;
+}
+
+int check_T(int T) {
+    if (T < 0 || T > BEAM_MOE_MAX_TOKENS) return fail(BEAM_MOE_ERR_ARG, "T=%d must be in [0, %d]", T, BEAM_MOE_MAX_TOKENS);
+    return BEAM_MOE_OK;
+}
+
+int check_ptr(const void* p, const char* name) {
+    if (!p) return fail(BEAM_MOE_ERR_ARG, "%s is null", name);
+    if (reinterpret_cast<uintptr_t>(p) % 16) return fail(BEAM_MOE_ERR_ALIGN, "%s is not 16-byte aligned", name);
+    return BEAM_MOE_OK;
+}
+
+Shape shape_of(const beam_moe_config* c) { return Shape{c->d, c->I, c->E, c->n_group, c->topk_group, c->top_k, c->scale}; }
+
+struct Scratch {
+    float* partial = nullptr;
+    int32_t* idx = nullptr;
+    float* w = nullptr;
+    int* chunk = nullptr;
+    int* expert_offset = nullptr;
+    int4* tiles = nullptr;
+    int* perm_src = nullptr;
+    int* inv_slot = nullptr;
+    bf16* x_perm = nullptr;
+    bf16* h = nullptr;
+    float* y = nullptr;
+};
+
+struct Carver {
+    char* base;
+    size_t off = 0;
+    template <typename T>
+    T* take(size_t count) {
+        off = (off + 255) & ~size_t(255);
+        T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+// Lays scratch out from `base` (nullptr: size only). Returns the byte count.
+size_t layout(const Shape& s, int T, int splits, int max_tiles, bool forward, bool route_out, char* base,
+              Scratch* sc) {
+    Carver c{base};
+    const size_t pairs = static_cast<size_t>(T) * s.top_k;
+    sc->partial = c.take<float>(static_cast<size_t>(splits) * T * s.E);
+    if (route_out) {
+        sc->idx = c.take<int32_t>(pairs);
+        sc->w = c.take<float>(pairs);
+    }
+    if (forward) {
+        const int nchunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+        sc->chunk = c.take<int>(static_cast<size_t>(nchunks) * s.E);
+        sc->expert_offset = c.take<int>(s.E + 1);
+        sc->tiles = c.take<int4>(1 + static_cast<size_t>(max_tiles));
+        sc->perm_src = c.take<int>(pairs);
+        sc->inv_slot = c.take<int>(pairs);
+        sc->x_perm = c.take<bf16>(pairs * s.d);
+        sc->h = c.take<bf16>(pairs * s.I);
+        sc->y = c.take<float>(pairs * s.d);
+    }
+    return c.off + 256;
+}
+
+#define LAUNCH(stage, expr)                                                                         \
+    do {                                                                                            \
+        stage_begin(stage, st);                                                                     \
+        cudaError_t e_ = (expr);                                                                    \
+        stage_end(stage, st);                                                                       \
+        if (e_ != cudaSuccess) {                                                                    \
+            rc = fail(BEAM_MOE_ERR_CUDA, "launch of %s failed: %s", #stage, cudaGetErrorString(e_)); \
+            goto done;                                                                              \
+        }                                                                                           \
+    } while (0)
+
+// mode 0: route (outputs topk_idx/topk_w); 1: logits only; 2: forward.
+int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float* bias, const bf16* wg,
+        const bf16* wu, const bf16* wd, int T, int32_t* topk_idx, float* topk_w, float* logits, bf16* out, int mode,
+        cudaStream_t st) {
+    g_launches = 0;
+    timing_begin_call();
+    int rc;
+    if ((rc = check_cfg(cfg)) || (rc = check_T(T)) || (rc = check_ptr(x, "x")) || (rc = check_ptr(wr, "router_w")))
+        return rc;
+    if (mode != 1 && (rc = check_ptr(bias, "expert_bias"))) return rc;
+    if (mode == 0 && ((rc = check_ptr(topk_idx, "topk_idx")) || (rc = check_ptr(topk_w, "topk_w")))) return rc;
+    if (mode == 1 && (rc = check_ptr(logits, "logits"))) return rc;
+    if (mode == 2 && ((rc = check_ptr(wg, "w_gate")) || (rc = check_ptr(wu, "w_up")) ||
+                      (rc = check_ptr(wd, "w_down")) || (rc = check_ptr(out, "out"))))
+        return rc;
+    if (T == 0) return BEAM_MOE_OK;
+    if ((rc = check_stream(st))) return rc;
+    DeviceState* dev = nullptr;
+    if ((rc = device_state(&dev))) return rc;
+
+    if (g_timing.enabled) {
+        int d = -1;
+        cudaGetDevice(&d);
+        if (g_timing.created && g_timing.device != d) {
+            for (int i = 0; i < kNumStages; ++i) {
+                cudaEventDestroy(g_timing.start[i]);
+                cudaEventDestroy(g_timing.stop[i]);
+            }
+            g_timing.created = false;
+        }
+        if (!g_timing.created) {
+            for (int i = 0; i < kNumStages; ++i) {
+                cudaEventCreate(&g_timing.start[i]);
+                cudaEventCreate(&g_timing.stop[i]);
+            }
+            g_timing.created = true;
+            g_timing.device = d;
+        }
+    }
+
+    const Shape s = shape_of(cfg);
+    const int splits = router_splits(s, T, dev->num_sms);
+    const int bn_max = gemm_bn_max(T);
+    const int max_tiles = dispatch_max_tiles(s, T, bn_max);
+    const int rows = T * s.top_k;
+    Scratch sc;
+    const size_t bytes = layout(s, T, splits, max_tiles, mode == 2, mode != 0, nullptr, &sc);
+    void* mem = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, st);
+    if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "scratch allocation of %zu bytes: %s", bytes, cudaGetErrorString(e));
+    layout(s, T, splits, max_tiles, mode == 2, mode != 0, static_cast<char*>(mem), &sc);
+    {
+        int32_t* idx = mode == 0 ? topk_idx : sc.idx;
+        float* w = mode == 0 ? topk_w : sc.w;
+        LAUNCH(kLogits, launch_router_logits(s, x, wr, T, splits, sc.partial, st));
+        LAUNCH(kSelect, launch_router_select(s, sc.partial, splits, mode == 1 ? nullptr : bias, T, idx, w,
+                                             mode == 1 ? logits : nullptr, st));
+        if (mode == 2) {
+            LAUNCH(kCount, launch_dispatch_count(s, idx, T, sc.chunk, dev->status, st));
+            LAUNCH(kScan, launch_dispatch_scan(s, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, st));
+            LAUNCH(kScatter, launch_dispatch_scatter(s, idx, T, sc.chunk, sc.perm_src, sc.inv_slot, dev->status, st));
+            LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, rows, sc.x_perm, dev->status, dev->num_sms, st));
+            LAUNCH(kGateUp, launch_gateup(s, wg, wu, sc.x_perm, rows, sc.tiles, max_tiles, bn_max, sc.h, dev->status,
+                                          dev->num_sms, st));
+            LAUNCH(kDown, launch_down(s, wd, sc.h, rows, sc.tiles, max_tiles, bn_max, sc.y, dev->status,
+                                      dev->num_sms, st));
+            LAUNCH(kCombine, launch_combine(s, sc.y, sc.inv_slot, w, T, out, dev->status, st));
+        }
+    }
+    rc = BEAM_MOE_OK;
+done:
+    e = cudaFreeAsync(mem, st);
+    if (rc == BEAM_MOE_OK && e != cudaSuccess)
+        rc = fail(BEAM_MOE_ERR_CUDA, "scratch release: %s", cudaGetErrorString(e));
+    return rc;
+}
+
+}  // namespace
+}  // namespace beam
+
+using namespace beam;
+
+extern "C" {
+
+beam_moe_config beam_moe_default_config(void) {
+    beam_moe_config c;
+    c.d = 5120;
+    c.I = 2560;
+    c.E = 256;
+    c.n_group = 8;
+    c.topk_group = 4;
+    c.top_k = 8;
+    c.scale = 2.5f;
+    return c;
+}
+
+int beam_moe_route_ex(const beam_moe_config* cfg, const __nv_bfloat16* x, const float* router_w,
+                      const float* expert_bias, int T, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
+    return run(cfg, x, router_w, expert_bias, nullptr, nullptr, nullptr, T, topk_idx, topk_w, nullptr, nullptr, 0,
+               stream);
+}
+
+int beam_moe_route(const __nv_bfloat16* x, const float* router_w, const float* expert_bias, int T, int32_t* topk_idx,
+                   float* topk_w, cudaStream_t stream) {
+    const beam_moe_config c = beam_moe_default_config();
+    return beam_moe_route_ex(&c, x, router_w, expert_bias, T, topk_idx, topk_w, stream);
+}
+
+int beam_moe_forward_ex(const beam_moe_config* cfg, const __nv_bfloat16* x, const float* router_w,
+                        const float* expert_bias, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
+                        const __nv_bfloat16* w_down, int T, __nv_bfloat16* out, cudaStream_t stream) {
+    return run(cfg, x, router_w, expert_bias, w_gate, w_up, w_down, T, nullptr, nullptr, nullptr, out, 2, stream);
+}
+
+int beam_moe_forward(const __nv_bfloat16* x, const float* router_w, const float* expert_bias,
+                     const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up, const __nv_bfloat16* w_down, int T,
+                     __nv_bfloat16* out, cudaStream_t stream) {
+    const beam_moe_config c = beam_moe_default_config();
+    return beam_moe_forward_ex(&c, x, router_w, expert_bias, w_gate, w_up, w_down, T, out, stream);
+}
+
+int beam_moe_router_logits(const beam_moe_config* cfg, const __nv_bfloat16* x, const float* router_w, int T,
+                           float* logits, cudaStream_t stream) {
+    return run(cfg, x, router_w, nullptr, nullptr, nullptr, nullptr, T, nullptr, nullptr, logits, nullptr, 1, stream);
+}
+
+const char* beam_moe_last_error(void) { return g_err; }
+
+int beam_moe_device_status(cudaStream_t stream) {
+    int rc;
+    if ((rc = check_stream(stream))) return rc;
+    DeviceState* dev = nullptr;
+    if ((rc = device_state(&dev))) return rc;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    int word = 0;
+    if ((e = cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail(BEAM_MOE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (word == kStatusOk) return BEAM_MOE_OK;
+    cudaMemset(dev->status, 0, sizeof word);
+    return fail(BEAM_MOE_ERR_DEVICE, "kernel status %d (%s)", word,
+                word == kStatusBadExpert    ? "expert index out of range in dispatch"
+                : word == kStatusWaitTimeout ? "a GEMM pipeline wait ran past its limit"
+                : word == kStatusBadIndex    ? "a permuted row or work-list index out of range (access skipped)"
+                                             : "unknown");
+}
+
+int beam_moe_timing_enable(int enable) {
+    g_timing.enabled = enable != 0;
+    return BEAM_MOE_OK;
+}
+
+int beam_moe_timing_read(float* ms, int max_stages) {
+    if (!ms || max_stages < 0) return fail(BEAM_MOE_ERR_ARG, "bad timing buffer");
+    if (g_timing.last) {
+        cudaError_t e = cudaEventSynchronize(g_timing.last);
+        if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "event synchronize: %s", cudaGetErrorString(e));
+    }
+    for (int i = 0; i < max_stages && i < kNumStages; ++i) {
+        float v = 0.f;
+        if (g_timing.ran[i] && cudaEventElapsedTime(&v, g_timing.start[i], g_timing.stop[i]) != cudaSuccess) v = 0.f;
+        ms[i] = v;
+    }
+    return kNumStages;
+}
+
+int beam_moe_last_launch_count(void) { return g_launches; }
+
+}  // extern "C"

@@ -1,0 +1,198 @@
+// Dispatch: group the T*top_k (token, slot) pairs by expert, in token order within each
+// expert, without order-dependent atomics, so the permutation is the same on every run.
+//
+// Tokens are taken in chunks of 256. For each chunk, a shared-memory bitmap holds one bit
+// per (expert, token of the chunk); it is built with atomicOr, whose result does not
+// depend on the order of the ORs. The rank of token t among the chunk's tokens routed to
+// expert e is the popcount of e's bits below t.
+//   count:   per-chunk expert histogram from the bitmap;
+//   scan:    per expert, exclusive scan over chunks; then an exclusive scan over experts
+//            gives each expert's first permuted row; also emits the GEMM work list of
+//            N-tiles (at most bn_max rows each, split evenly);
+//   scatter: permuted row of (t, k) = chunk base of e + rank; writes perm_src[row] = t
+//            and inv_slot[t, k] = row;
+//   gather:  x_perm[row] = x[perm_src[row]] with 16-byte loads and stores.
+#include "internal.cuh"
+
+namespace beam {
+namespace {
+
+constexpr int kChunk = kDispatchChunk;
+constexpr int kWords = kChunk / 32;
+
+__device__ __forceinline__ void build_bitmap(uint32_t* bm, const int32_t* __restrict__ idx, int T, int E, int K,
+                                             int t0, int* status) {
+    for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) bm[i] = 0u;
+    __syncthreads();
+    const int tl = threadIdx.x;
+    const int t = t0 + tl;
+    if (t < T) {
+        for (int k = 0; k < K; ++k) {
+            const int e = idx[static_cast<size_t>(t) * K + k];
+            if (e < 0 || e >= E) {
+                atomicCAS(status, 0, kStatusBadExpert);
+                continue;
+            }
+            atomicOr(&bm[e * kWords + (tl >> 5)], 1u << (tl & 31));
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kChunk) dispatch_count_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
+                                                                int* __restrict__ chunk_count, int* status) {
+    extern __shared__ uint32_t bm[];
+    build_bitmap(bm, idx, T, E, K, blockIdx.x * kChunk, status);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int n = 0;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) n += __popc(bm[e * kWords + w]);
+        chunk_count[static_cast<size_t>(blockIdx.x) * E + e] = n;
+    }
+}
+
+// One block of 1024 threads; thread e < E owns expert e.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int nchunks, int E, int bn_max,
+                                                             int* __restrict__ chunk_count,
+                                                             int* __restrict__ expert_offset,
+                                                             int4* __restrict__ tiles) {
+    __shared__ int tot[1024];
+    __shared__ int ntl[1024];
+    const int e = threadIdx.x;
+    int n = 0;
+    if (e < E) {
+        for (int c = 0; c < nchunks; ++c) {
+            const int v = chunk_count[static_cast<size_t>(c) * E + e];
+            chunk_count[static_cast<size_t>(c) * E + e] = n;
+            n += v;
+        }
+    }
+    // N-tiles of expert e: an even split into pieces of `per` rows (a multiple of 16,
+    // at most bn_max); the last piece takes the remainder.
+    int per = 0, nt = 0;
+    if (n > 0) {
+        const int q = (n + bn_max - 1) / bn_max;
+        per = min(bn_max, (((n + q - 1) / q + 15) / 16) * 16);
+        nt = (n + per - 1) / per;
+    }
+    tot[e] = n;
+    ntl[e] = nt;
+    __syncthreads();
+    // Inclusive Hillis-Steele scans of expert totals and tile counts.
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int a = e >= off ? tot[e - off] : 0;
+        const int b = e >= off ? ntl[e - off] : 0;
+        __syncthreads();
+        tot[e] += a;
+        ntl[e] += b;
+        __syncthreads();
+    }
+    if (e < E) {
+        const int base = tot[e] - n;   // first permuted row of expert e
+        expert_offset[e] = base;
+        if (e == E - 1) {
+            expert_offset[E] = tot[e];
+            tiles[0] = make_int4(ntl[e], 0, 0, 0);
+        }
+        for (int c = 0; c < nchunks; ++c) chunk_count[static_cast<size_t>(c) * E + e] += base;
+        if (nt > 0) {
+            int tile = ntl[e] - nt;
+            for (int r = 0; r < n; r += per) {
+                const int rows = min(per, n - r);
+                tiles[1 + tile++] = make_int4(e, base + r, rows, 0);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(const int32_t* __restrict__ idx, int T, int E,
+                                                                  int K, const int* __restrict__ chunk_base,
+                                                                  int* __restrict__ perm_src,
+                                                                  int* __restrict__ inv_slot, int* status) {
+    extern __shared__ uint32_t bm[];
+    const int t0 = blockIdx.x * kChunk;
+    build_bitmap(bm, idx, T, E, K, t0, status);
+    const int tl = threadIdx.x;
+    const int t = t0 + tl;
+    if (t >= T) return;
+    const int w = tl >> 5;
+    const uint32_t below = (1u << (tl & 31)) - 1u;
+    for (int k = 0; k < K; ++k) {
+        const int e = idx[static_cast<size_t>(t) * K + k];
+        if (e < 0 || e >= E) continue;
+        int rank = __popc(bm[e * kWords + w] & below);
+        for (int j = 0; j < w; ++j) rank += __popc(bm[e * kWords + j]);
+        const int row = chunk_base[static_cast<size_t>(blockIdx.x) * E + e] + rank;
+        if (row < 0 || row >= T * K) {
+            atomicCAS(status, 0, kStatusBadIndex);
+            continue;
+        }
+        inv_slot[static_cast<size_t>(t) * K + k] = row;
+        perm_src[row] = t;
+    }
+}
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int row_vecs, int T,
+                                                          const int* __restrict__ perm_src, int rows,
+                                                          uint4* __restrict__ x_perm, int* status) {
+    const size_t total = static_cast<size_t>(rows) * row_vecs;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t r = i / row_vecs;
+        const size_t v = i - r * row_vecs;
+        const int src = perm_src[r];
+        if (static_cast<unsigned>(src) >= static_cast<unsigned>(T)) {
+            atomicCAS(status, 0, kStatusBadIndex);
+            continue;
+        }
+        x_perm[i] = x[static_cast<size_t>(src) * row_vecs + v];
+    }
+}
+
+}  // namespace
+
+int dispatch_max_tiles(const Shape& s, int T, int bn_max) {
+    const long long pairs = static_cast<long long>(T) * s.top_k;
+    const long long used = pairs < s.E ? pairs : s.E;
+    return static_cast<int>(pairs / bn_max + used + 1);
+}
+
+cudaError_t launch_dispatch_count(const Shape& s, const int32_t* topk_idx, int T, int* chunk_count, int* status,
+                                  cudaStream_t st) {
+    const int nchunks = (T + kChunk - 1) / kChunk;
+    const size_t smem = static_cast<size_t>(s.E) * kWords * sizeof(uint32_t);
+    dispatch_count_kernel<<<nchunks, kChunk, smem, st>>>(topk_idx, T, s.E, s.top_k, chunk_count, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scan(const Shape& s, int T, int bn_max, int* chunk_count, int* expert_offset, int4* tiles,
+                                 cudaStream_t st) {
+    const int nchunks = (T + kChunk - 1) / kChunk;
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(nchunks, s.E, bn_max, chunk_count, expert_offset, tiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scatter(const Shape& s, const int32_t* topk_idx, int T, const int* chunk_base,
+                                    int* perm_src, int* inv_slot, int* status, cudaStream_t st) {
+    const int nchunks = (T + kChunk - 1) / kChunk;
+    const size_t smem = static_cast<size_t>(s.E) * kWords * sizeof(uint32_t);
+    dispatch_scatter_kernel<<<nchunks, kChunk, smem, st>>>(topk_idx, T, s.E, s.top_k, chunk_base, perm_src, inv_slot,
+                                                           status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, int rows, bf16* x_perm,
+                               int* status, int num_sms, cudaStream_t st) {
+    const int row_vecs = d / 8;
+    const long long total = static_cast<long long>(rows) * row_vecs;
+    long long blocks = (total + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const uint4*>(x), row_vecs, T,
+                                                                      perm_src, rows,
+                                                                      reinterpret_cast<uint4*>(x_perm), status);
+    return cudaGetLastError();
+}
+
+}  // namespace beam

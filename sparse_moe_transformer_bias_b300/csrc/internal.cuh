@@ -1,0 +1,63 @@
+// Declarations shared by the kernels' host launchers and the C-ABI layer.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace beam {
+
+using bf16 = __nv_bfloat16;
+
+struct Shape {
+    int d, I, E, n_group, topk_group, top_k;
+    float scale;
+};
+
+// Device status codes written to the status word (first error wins).
+enum : int { kStatusOk = 0, kStatusBadExpert = 1, kStatusWaitTimeout = 2, kStatusBadIndex = 3 };
+
+// One N-tile of the grouped GEMMs: `rows` consecutive permuted rows starting at `row0`,
+// all routed to expert `e`. The work list is int4 {e, row0, rows, 0} after an int4 header
+// whose .x is the tile count.
+constexpr int kDispatchChunk = 256;  // tokens per dispatch block
+
+// ---------------------------------------------------------------- router (router.cu)
+int router_splits(const Shape& s, int T, int num_sms);
+cudaError_t launch_router_logits(const Shape& s, const bf16* x, const float* wr, int T, int splits, float* partial,
+                                 cudaStream_t st);
+cudaError_t launch_router_select(const Shape& s, const float* partial, int splits, const float* bias, int T,
+                                 int32_t* topk_idx, float* topk_w, float* logits_out, cudaStream_t st);
+
+// ---------------------------------------------------------------- dispatch (dispatch.cu)
+int dispatch_max_tiles(const Shape& s, int T, int bn_max);
+cudaError_t launch_dispatch_count(const Shape& s, const int32_t* topk_idx, int T, int* chunk_count, int* status,
+                                  cudaStream_t st);
+cudaError_t launch_dispatch_scan(const Shape& s, int T, int bn_max, int* chunk_count, int* expert_offset,
+                                 int4* tiles, cudaStream_t st);
+cudaError_t launch_dispatch_scatter(const Shape& s, const int32_t* topk_idx, int T, const int* chunk_base,
+                                    int* perm_src, int* inv_slot, int* status, cudaStream_t st);
+cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, int rows, bf16* x_perm,
+                               int* status, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- grouped GEMMs (grouped_gemm.cu)
+// Largest N-tile (tokens per tile) the GEMMs use for a batch of T tokens.
+int gemm_bn_max(int T);
+// h[rows, I] = silu(x_perm . Wg[e]^T) * (x_perm . Wu[e]^T), per N-tile of the work list.
+cudaError_t launch_gateup(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* x_perm, int rows,
+                          const int4* tiles, int max_tiles, int bn_max, bf16* h, int* status, int num_sms,
+                          cudaStream_t st);
+// y[rows, d] = h . Wd[e]^T (FP32), per N-tile of the work list.
+cudaError_t launch_down(const Shape& s, const bf16* w_down, const bf16* h, int rows, const int4* tiles, int max_tiles,
+                        int bn_max, float* y, int* status, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- combine (combine.cu)
+cudaError_t launch_combine(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T, bf16* out,
+                           int* status, cudaStream_t st);
+
+// Host helper: encode a 2-D BF16 tensor map (rows x cols, row-major) with the 128-byte
+// swizzle and a box of box_cols x box_rows. Returns false if the driver refuses it.
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                         uint32_t box_cols, const char** why);
+
+}  // namespace beam

@@ -1,0 +1,70 @@
+"""Tensor-level calls over the C ABI: allocate outputs, check shapes, call the library.
+
+    out = moe.forward(x, router_w, bias, w_gate, w_up, w_down)          # Beam shape
+    idx, w = moe.route(x, router_w, bias, shape=workloads.TINY)
+    logits = moe.router_logits(x, router_w)
+    out = moe.forward_host(x_pinned, ...)     # host in, host out (copies on the stream)
+
+All compute runs in libbeam_moe.so; nothing here touches the numbers.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import abi
+from .workloads import BEAM, MoEShape
+
+
+def _check_inputs(shape: MoEShape, x, router_w, bias=None):
+    T = x.shape[0]
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.shape == (T, shape.d) and x.is_contiguous()
+    assert router_w.dtype == torch.float32 and router_w.shape == (shape.E, shape.d) and router_w.is_contiguous()
+    if bias is not None:
+        assert bias.dtype == torch.float32 and bias.shape == (shape.E,) and bias.is_contiguous()
+    return T
+
+
+def route(x, router_w, bias, shape: MoEShape = BEAM, stream=None):
+    T = _check_inputs(shape, x, router_w, bias)
+    idx = torch.empty((T, shape.top_k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, shape.top_k), dtype=torch.float32, device=x.device)
+    abi.beam_moe_route_ex(shape, x, router_w, bias, T, idx, w, stream)
+    return idx, w
+
+
+def router_logits(x, router_w, shape: MoEShape = BEAM, stream=None):
+    T = _check_inputs(shape, x, router_w)
+    logits = torch.empty((T, shape.E), dtype=torch.float32, device=x.device)
+    abi.beam_moe_router_logits(shape, x, router_w, T, logits, stream)
+    return logits
+
+
+def forward(x, router_w, bias, w_gate, w_up, w_down, shape: MoEShape = BEAM, out=None, stream=None):
+    T = _check_inputs(shape, x, router_w, bias)
+    for w, rows, cols in ((w_gate, shape.I, shape.d), (w_up, shape.I, shape.d), (w_down, shape.d, shape.I)):
+        assert w.dtype == torch.bfloat16 and w.shape == (shape.E, rows, cols) and w.is_contiguous()
+    if out is None:
+        out = torch.empty((T, shape.d), dtype=torch.bfloat16, device=x.device)
+    abi.beam_moe_forward_ex(shape, x, router_w, bias, w_gate, w_up, w_down, T, out, stream)
+    return out
+
+
+def forward_host(x_host, router_w, bias, w_gate, w_up, w_down, shape: MoEShape = BEAM, x_dev=None, out_dev=None,
+                 out_host=None, stream=None):
+    """Host tokens in, host output out: copies x to the device, runs the block, copies
+    the output back, all on `stream`; returns out_host once the stream has finished."""
+    stream = stream or torch.cuda.current_stream()
+    T = x_host.shape[0]
+    dev = router_w.device
+    if x_dev is None:
+        x_dev = torch.empty((T, shape.d), dtype=torch.bfloat16, device=dev)
+    if out_dev is None:
+        out_dev = torch.empty((T, shape.d), dtype=torch.bfloat16, device=dev)
+    if out_host is None:
+        out_host = torch.empty((T, shape.d), dtype=torch.bfloat16, pin_memory=True)
+    with torch.cuda.stream(stream):
+        x_dev.copy_(x_host, non_blocking=True)
+        forward(x_dev, router_w, bias, w_gate, w_up, w_down, shape, out=out_dev, stream=stream)
+        out_host.copy_(out_dev, non_blocking=True)
+    stream.synchronize()
+    return out_host

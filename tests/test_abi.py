@@ -1,0 +1,94 @@
+"""The C-ABI library loads, exports every declared symbol and rejects bad arguments on
+the host (no GPU needed: every call here fails or returns before touching the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_moe_transformer_bias_b300 import abi, build, workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "beam_moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return abi.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"BEAM_MOE_API\s+[\w\s\*]*?\b(beam_moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_symbols() == sorted(abi.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_default_config_is_beam(lib):
+    c = abi.beam_moe_default_config()
+    assert (c.d, c.I, c.E, c.n_group, c.topk_group, c.top_k, c.scale) == (5120, 2560, 256, 8, 4, 8, 2.5)
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced by argument checks
+
+
+def call_forward(cfg, T=4, x=FAKE, wr=FAKE, b=FAKE, wg=FAKE, wu=FAKE, wd=FAKE, out=FAKE):
+    return lib_().beam_moe_forward_ex(ctypes.byref(cfg), x, wr, b, wg, wu, wd, T, out, None)
+
+
+def lib_():
+    return abi.load()
+
+
+def cfg_of(**kw):
+    base = dict(d=5120, I=2560, E=256, n_group=8, topk_group=4, top_k=8, scale=2.5)
+    base.update(kw)
+    return abi.BeamMoeConfig(**base)
+
+
+@pytest.mark.parametrize("kw,what", [
+    (dict(d=5000), "d=5000"), (dict(I=100), "I=100"), (dict(E=250), "E=250"), (dict(n_group=9, E=288), "n_group"),
+    (dict(topk_group=9), "topk_group"), (dict(topk_group=0), "topk_group"), (dict(top_k=0), "top_k"),
+    (dict(top_k=33), "top_k"), (dict(scale=float("inf")), "scale"),
+])
+def test_bad_config_rejected(lib, kw, what):
+    assert call_forward(cfg_of(**kw)) == abi.BEAM_MOE_ERR_ARG
+    assert what.split("=")[0] in abi.beam_moe_last_error()
+
+
+def test_bad_token_count_rejected(lib):
+    assert call_forward(cfg_of(), T=-1) == abi.BEAM_MOE_ERR_ARG
+    assert call_forward(cfg_of(), T=abi.BEAM_MOE_MAX_TOKENS + 1) == abi.BEAM_MOE_ERR_ARG
+
+
+@pytest.mark.parametrize("arg", ["x", "wr", "b", "wg", "wu", "wd", "out"])
+def test_null_and_misaligned_pointers_rejected(lib, arg):
+    assert call_forward(cfg_of(), **{arg: None}) == abi.BEAM_MOE_ERR_ARG
+    assert "null" in abi.beam_moe_last_error()
+    assert call_forward(cfg_of(), **{arg: FAKE + 8}) == abi.BEAM_MOE_ERR_ALIGN
+    assert "aligned" in abi.beam_moe_last_error()
+
+
+def test_zero_tokens_is_a_no_op(lib):
+    assert call_forward(cfg_of(), T=0) == abi.BEAM_MOE_OK
+    assert lib.beam_moe_route_ex(ctypes.byref(cfg_of(**dict(d=512, I=256))), FAKE, FAKE, FAKE, 0, FAKE, FAKE,
+                                 None) == abi.BEAM_MOE_OK
+    assert lib.beam_moe_router_logits(ctypes.byref(cfg_of()), FAKE, FAKE, 0, FAKE, None) == abi.BEAM_MOE_OK
+    assert abi.beam_moe_last_launch_count() == 0
+
+
+def test_binding_raises_with_message(lib):
+    with pytest.raises(abi.BeamMoeError, match="T=-3"):
+        abi.beam_moe_route_ex(W.TINY, FAKE, FAKE, FAKE, -3, FAKE, FAKE, stream=0)
+
+
+def test_tiny_shape_accepted_by_checks(lib):
+    assert call_forward(abi.BeamMoeConfig.of(W.TINY), T=0) == abi.BEAM_MOE_OK

@@ -1,0 +1,146 @@
+"""Forward parity: the CUDA MoE block against the CPU oracle, element by element, on Tiny
+(every token, ragged token counts) and on Beam shapes (sampled tokens at full size, in the
+same launch configuration the benchmark times), plus closed-form and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import parity as P
+from sparse_moe_transformer_bias_b300 import abi, moe, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(layer):
+    shape = layer.shape
+    out = moe.forward(layer.x, layer.wr, layer.b, layer.wg, layer.wu, layer.wd, shape)
+    logits = moe.router_logits(layer.x, layer.wr, shape)
+    idx, _ = moe.route(layer.x, layer.wr, layer.b, shape)
+    abi.beam_moe_device_status()
+    return out.float().cpu().numpy(), logits.cpu().numpy(), idx.cpu().numpy()
+
+
+def check_layer(layer, tokens, what):
+    out, logits, idx = run_gpu(layer)
+    ref, flagged = P.oracle_forward_for(layer, tokens, logits, idx)
+    frob = P.check_output(out[np.asarray(tokens)], ref, what)
+    print(f"{what}: tokens checked {len(tokens)}, near-tie {len(flagged)}, rel frob {frob:.2e}")
+    return out, idx
+
+
+def tiny_layer(T, seed=0):
+    shape = W.TINY
+    x = W.make_tokens(shape, T, seed, "cuda")
+    wr, b = W.make_router(shape, seed, "cuda")
+    wg, wu, wd = W.make_experts(shape, seed, "cuda")
+    return P.Layer(shape, x, wr, b, wg, wu, wd)
+
+
+@pytest.mark.parametrize("T", [1, 7, 128, 129, 300])
+def test_tiny_forward_parity(T):
+    layer = tiny_layer(T)
+    check_layer(layer, np.arange(T), f"tiny T={T}")
+
+
+@pytest.mark.parametrize("name,T,hot,n_check", [
+    ("decode", 16, 0, 16),
+    ("sweep_T1", 1, 0, 1),
+    ("sweep_T8", 8, 0, 8),
+    ("sweep_T64", 64, 0, 16),
+    ("sweep_T256", 256, 0, 16),
+    ("sweep_T1024", 1024, 0, 16),
+    ("prefill", 4096, 0, 32),
+    ("sweep_T16384", 16384, 0, 16),
+    ("skewed", 32768, 16, 48),
+])
+def test_beam_forward_parity(beam_experts, beam_host_cache, name, T, hot, n_check):
+    shape = W.BEAM
+    x = W.make_tokens(shape, T, 0, "cuda")
+    wr, b = W.make_router(shape, 0, "cuda", hot_experts=hot)
+    layer = P.Layer(shape, x, wr, b, *beam_experts, host_cache=beam_host_cache)
+    tokens = W.sample_tokens(T, n_check, seed=2).numpy()
+    if T > n_check:
+        tokens = np.unique(np.concatenate([tokens, [T - 1]]))  # always include the ragged tail
+    _, idx = check_layer(layer, tokens, f"{name} T={T}")
+    if hot:
+        load = np.bincount(idx.ravel(), minlength=shape.E)
+        assert load.max() > 10 * load.mean()
+        # check tokens routed to the hottest expert too (its N-tiles split many ways)
+        hottest = int(load.argmax())
+        rows = np.nonzero((idx == hottest).any(axis=1))[0]
+        pick = rows[np.linspace(0, len(rows) - 1, 8).astype(int)]
+        check_layer(layer, pick, f"{name} hot expert {hottest} ({load.max()} tokens)")
+
+
+def test_zero_input_gives_zero_output():
+    """x = 0 and equal biases: every score ties, so experts 0..7 with weights 2.5/8, and
+    every expert output is 0."""
+    layer = tiny_layer(9)
+    layer.x = torch.zeros_like(layer.x)
+    layer.b = torch.full_like(layer.b, 0.03)
+    out, _, idx = run_gpu(layer)
+    assert (out == 0).all()
+    assert (idx == np.arange(8)[None, :]).all()
+
+
+def test_identical_experts_closed_form():
+    """All experts equal: output = 2.5 * expert(x), with expert(x) from torch float64."""
+    layer = tiny_layer(40, seed=5)
+    E = layer.shape.E
+    for w in (layer.wg, layer.wu, layer.wd):
+        w.copy_(w[3:4].expand(E, -1, -1))
+    out, _, _ = run_gpu(layer)
+    x64 = layer.x.double().cpu()
+    g = x64 @ layer.wg[3].double().cpu().T
+    u = x64 @ layer.wu[3].double().cpu().T
+    ref = 2.5 * ((torch.nn.functional.silu(g) * u) @ layer.wd[3].double().cpu().T)
+    P.check_output(out, ref.numpy(), "identical experts")
+
+
+def test_forward_deterministic():
+    layer = tiny_layer(300, seed=7)
+    a = moe.forward(layer.x, layer.wr, layer.b, layer.wg, layer.wu, layer.wd, layer.shape)
+    c = moe.forward(layer.x, layer.wr, layer.b, layer.wg, layer.wu, layer.wd, layer.shape)
+    torch.cuda.synchronize()
+    assert torch.equal(a, c)
+
+
+def test_zero_tokens_launch_nothing():
+    layer = tiny_layer(1)
+    out = torch.empty((1, layer.shape.d), dtype=torch.bfloat16, device="cuda")
+    abi.beam_moe_forward_ex(layer.shape, layer.x, layer.wr, layer.b, layer.wg, layer.wu, layer.wd, 0, out)
+    assert abi.beam_moe_last_launch_count() == 0
+
+
+def test_launch_count_and_stage_timing():
+    layer = tiny_layer(64)
+    abi.beam_moe_timing_enable(True)
+    try:
+        moe.forward(layer.x, layer.wr, layer.b, layer.wg, layer.wu, layer.wd, layer.shape)
+        n = abi.beam_moe_last_launch_count()
+        times = abi.beam_moe_timing_read()
+    finally:
+        abi.beam_moe_timing_enable(False)
+    assert n == len(abi.STAGES)
+    assert all(v > 0 for v in times.values()), times
+
+
+def test_host_buffers_end_to_end():
+    layer = tiny_layer(33)
+    x_host = layer.x.cpu().pin_memory()
+    out_host = moe.forward_host(x_host, layer.wr, layer.b, layer.wg, layer.wu, layer.wd, layer.shape)
+    ref = moe.forward(layer.x, layer.wr, layer.b, layer.wg, layer.wu, layer.wd, layer.shape).cpu()
+    assert torch.equal(out_host, ref)
+
+
+def test_device_status_clean():
+    assert abi.beam_moe_device_status() == abi.BEAM_MOE_OK
+
+
+def test_product_path_is_the_cuda_library():
+    """The binding loads libbeam_moe.so and nothing of the oracle."""
+    import sparse_moe_transformer_bias_b300.abi as A
+    import sparse_moe_transformer_bias_b300.moe as M
+    for mod in (A, M):
+        assert "oracle" not in open(mod.__file__).read()
+    assert abi.load()._name == A.LIB_PATH
