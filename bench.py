@@ -39,9 +39,11 @@ METRIC = "Beam MoE-layer tokens/s (T=16 decode, T=4096 prefill); % of roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes (read + write) per launch of the dominant kernel from ncu captures; None when
-# the kernel changed after the capture. Keys: workload name.
-TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the dominant kernel from ncu captures (see
+# profiles/); remove an entry when its kernel changes after the capture. Keys: workload name.
+# decode: the E=32 capture read 52.6 MB per touched expert; scaled to the 89 experts the
+# decode batch touches.
+TRAFFIC = {"decode": {"kernel": "gateup_gemm", "bytes": 4.6813e9}}
 
 
 def peaks():
