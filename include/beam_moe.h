@@ -110,6 +110,26 @@ BEAM_MOE_API int beam_moe_forward_ex(const beam_moe_config *cfg, const __nv_bflo
                         const float *expert_bias, const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up,
                         const __nv_bfloat16 *w_down, int T, __nv_bfloat16 *out, cudaStream_t stream);
 
+/* Router with no device allocation. The release pages have no counterpart: this is a
+ * deployment variant of beam_moe_route_ex for callers that must not have a library
+ * allocate device memory (an engine that has claimed all free HBM for weights and KV
+ * cache, or a per-token path where an allocator call could synchronise the device or
+ * stall). Same arguments, layouts and results as beam_moe_route_ex; calls no cudaMalloc,
+ * cudaFree or pool allocation.
+ *   - Scratch: one fixed array of BEAM_MOE_NOALLOC_SCRATCH_BYTES in the library's device
+ *     image; every GPU that loads the library holds it until the process exits.
+ *   - Limit: T <= BEAM_MOE_NOALLOC_MAX_TOKENS, else BEAM_MOE_ERR_ARG with a message.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (every value a call
+ *     reads is written earlier in the same call). Calls that overlap on the GPU race on
+ *     it: serialise them (one stream, or events between streams).
+ *   - Not counted by beam_moe_last_launch_count or timed by beam_moe_timing_*. */
+#define BEAM_MOE_NOALLOC_MAX_TOKENS 8192
+#define BEAM_MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+BEAM_MOE_API int beam_moe_route_noalloc(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
+                           const float *expert_bias, int T, int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+
 /* Router logits only (output_router_logits in the transformers doc, Notes): the same
  * kernels as the router's first stage; logits fp32 [T, E]. */
 BEAM_MOE_API int beam_moe_router_logits(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w, int T,

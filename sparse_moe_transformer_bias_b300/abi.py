@@ -21,6 +21,8 @@ BEAM_MOE_ERR_ALIGN = -2
 BEAM_MOE_ERR_CUDA = -3
 BEAM_MOE_ERR_DEVICE = -4
 BEAM_MOE_MAX_TOKENS = 262144
+BEAM_MOE_NOALLOC_MAX_TOKENS = 8192
+BEAM_MOE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 STAGES = ("router_logits", "router_select", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather",
           "gateup_gemm", "down_gemm", "combine")
@@ -28,7 +30,8 @@ STAGES = ("router_logits", "router_select", "dispatch_count", "dispatch_scan", "
 # Every symbol include/beam_moe.h declares.
 EXPORTS = ("beam_moe_default_config", "beam_moe_route", "beam_moe_route_ex", "beam_moe_forward",
            "beam_moe_forward_ex", "beam_moe_router_logits", "beam_moe_last_error", "beam_moe_device_status",
-           "beam_moe_timing_enable", "beam_moe_timing_read", "beam_moe_last_launch_count")
+           "beam_moe_timing_enable", "beam_moe_timing_read", "beam_moe_last_launch_count",
+           "beam_moe_route_noalloc")
 
 
 class BeamMoeConfig(ctypes.Structure):
@@ -68,6 +71,7 @@ def load() -> ctypes.CDLL:
             L.beam_moe_forward.argtypes = [P, P, P, P, P, P, i, P, P]
             L.beam_moe_forward_ex.argtypes = [cfgp, P, P, P, P, P, P, i, P, P]
             L.beam_moe_router_logits.argtypes = [cfgp, P, P, i, P, P]
+            L.beam_moe_route_noalloc.argtypes = [cfgp, P, P, P, i, P, P, P]
             L.beam_moe_last_error.restype = ctypes.c_char_p
             L.beam_moe_last_error.argtypes = []
             L.beam_moe_device_status.argtypes = [P]
@@ -76,7 +80,7 @@ def load() -> ctypes.CDLL:
             L.beam_moe_last_launch_count.argtypes = []
             for f in ("beam_moe_route", "beam_moe_route_ex", "beam_moe_forward", "beam_moe_forward_ex",
                       "beam_moe_router_logits", "beam_moe_device_status", "beam_moe_timing_enable",
-                      "beam_moe_timing_read", "beam_moe_last_launch_count"):
+                      "beam_moe_timing_read", "beam_moe_last_launch_count", "beam_moe_route_noalloc"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -133,6 +137,13 @@ def beam_moe_forward(x, router_w, expert_bias, w_gate, w_up, w_down, T, out, str
 def beam_moe_forward_ex(cfg, x, router_w, expert_bias, w_gate, w_up, w_down, T, out, stream=None):
     return _check(load().beam_moe_forward_ex(_cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate),
                                              _ptr(w_up), _ptr(w_down), int(T), _ptr(out), _stream(stream)))
+
+
+def beam_moe_route_noalloc(cfg, x, router_w, expert_bias, T, topk_idx, topk_w, stream=None):
+    """beam_moe_route_ex without any device allocation (fixed scratch array in the
+    library; T <= BEAM_MOE_NOALLOC_MAX_TOKENS)."""
+    return _check(load().beam_moe_route_noalloc(_cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), int(T),
+                                                _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
 
 
 def beam_moe_router_logits(cfg, x, router_w, T, logits, stream=None):

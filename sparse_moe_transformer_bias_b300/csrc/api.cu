@@ -270,6 +270,18 @@ done:
 }
 
 }  // namespace
+
+int abi_fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+int abi_check_config(const beam_moe_config* cfg) { return check_cfg(cfg); }
+int abi_check_ptr(const void* p, const char* name) { return check_ptr(p, name); }
+int abi_check_stream(cudaStream_t st) { return check_stream(st); }
+
 }  // namespace beam
 
 using namespace beam;

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "beam_moe.h"
+
 namespace beam {
 
 using bf16 = __nv_bfloat16;
@@ -54,6 +56,14 @@ cudaError_t launch_down(const Shape& s, const bf16* w_down, const bf16* h, int r
 // ---------------------------------------------------------------- combine (combine.cu)
 cudaError_t launch_combine(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T, bf16* out,
                            int* status, cudaStream_t st);
+
+// ---------------------------------------------------------------- C-ABI helpers (api.cu)
+// The calling thread's error message (what beam_moe_last_error returns) and the argument
+// checks every entry point applies; each returns BEAM_MOE_OK or the failing code.
+int abi_fail(int code, const char* fmt, ...);
+int abi_check_config(const beam_moe_config* cfg);
+int abi_check_ptr(const void* p, const char* name);
+int abi_check_stream(cudaStream_t st);
 
 // Host helper: encode a 2-D BF16 tensor map (rows x cols, row-major) with the 128-byte
 // swizzle and a box of box_cols x box_rows. Returns false if the driver refuses it.
