@@ -126,7 +126,7 @@ BEAM_MOE_API int beam_moe_forward_ex(const beam_moe_config *cfg, const __nv_bflo
  *     it: serialise them (one stream, or events between streams).
  *   - Not counted by beam_moe_last_launch_count or timed by beam_moe_timing_*. */
 #define BEAM_MOE_NOALLOC_MAX_TOKENS 8192
-#define BEAM_MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define BEAM_MOE_NOALLOC_SCRATCH_BYTES (40u << 20)
 BEAM_MOE_API int beam_moe_route_noalloc(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
                            const float *expert_bias, int T, int32_t *topk_idx, float *topk_w, cudaStream_t stream);
 
@@ -147,9 +147,9 @@ BEAM_MOE_API int beam_moe_device_status(cudaStream_t stream);
 /* Per-stage timing for profiling. While enabled (per thread), each forward/route call
  * records CUDA events on its stream around each stage; beam_moe_timing_read synchronises
  * on the last call's final event and writes up to max_stages durations in milliseconds
- * (stage order: router logits, router select, dispatch count, dispatch scan, dispatch
- * scatter, gather, gate/up GEMM, down GEMM, combine; unrun stages read 0). Returns the
- * number of stages, or a negative error. */
+ * (stage order: router weight split, router logits, router select, dispatch count,
+ * dispatch scan, dispatch scatter, gather, gate/up GEMM, down GEMM, combine; unrun stages
+ * read 0). Returns the number of stages, or a negative error. */
 BEAM_MOE_API int beam_moe_timing_enable(int enable);
 BEAM_MOE_API int beam_moe_timing_read(float *ms, int max_stages);
 

@@ -22,9 +22,9 @@ BEAM_MOE_ERR_CUDA = -3
 BEAM_MOE_ERR_DEVICE = -4
 BEAM_MOE_MAX_TOKENS = 262144
 BEAM_MOE_NOALLOC_MAX_TOKENS = 8192
-BEAM_MOE_NOALLOC_SCRATCH_BYTES = 16 << 20
+BEAM_MOE_NOALLOC_SCRATCH_BYTES = 40 << 20
 
-STAGES = ("router_logits", "router_select", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather",
+STAGES = ("router_split", "router_logits", "router_select", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather",
           "gateup_gemm", "down_gemm", "combine")
 
 # Every symbol include/beam_moe.h declares.

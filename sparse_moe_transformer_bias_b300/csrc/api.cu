@@ -76,7 +76,7 @@ int check_stream(cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------- stage timing
-enum Stage { kLogits, kSelect, kCount, kScan, kScatter, kGather, kGateUp, kDown, kCombine, kNumStages };
+enum Stage { kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kGateUp, kDown, kCombine, kNumStages };
 struct Timing {
     bool enabled = false;
     bool created = false;
@@ -132,6 +132,7 @@ int check_ptr(const void* p, const char* name) {
 Shape shape_of(const beam_moe_config* c) { return Shape{c->d, c->I, c->E, c->n_group, c->topk_group, c->top_k, c->scale}; }
 
 struct Scratch {
+    bf16* w3 = nullptr;
     float* partial = nullptr;
     int32_t* idx = nullptr;
     float* w = nullptr;
@@ -158,11 +159,12 @@ struct Carver {
 };
 
 // Lays scratch out from `base` (nullptr: size only). Returns the byte count.
-size_t layout(const Shape& s, int T, int splits, int max_tiles, bool forward, bool route_out, char* base,
+size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool forward, bool route_out, char* base,
               Scratch* sc) {
     Carver c{base};
     const size_t pairs = static_cast<size_t>(T) * s.top_k;
-    sc->partial = c.take<float>(static_cast<size_t>(splits) * T * s.E);
+    sc->w3 = plan.w3_elems ? c.take<bf16>(plan.w3_elems) : nullptr;
+    sc->partial = c.take<float>(static_cast<size_t>(plan.splits) * T * s.E);
     if (route_out) {
         sc->idx = c.take<int32_t>(pairs);
         sc->w = c.take<float>(pairs);
@@ -233,21 +235,22 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     }
 
     const Shape s = shape_of(cfg);
-    const int splits = router_splits(s, T, dev->num_sms);
+    const RouterPlan plan = router_plan(s, T, dev->num_sms);
     const int bn_max = gemm_bn_max(T);
     const int max_tiles = dispatch_max_tiles(s, T, bn_max);
     const int rows = T * s.top_k;
     Scratch sc;
-    const size_t bytes = layout(s, T, splits, max_tiles, mode == 2, mode != 0, nullptr, &sc);
+    const size_t bytes = layout(s, T, plan, max_tiles, mode == 2, mode != 0, nullptr, &sc);
     void* mem = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, st);
     if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "scratch allocation of %zu bytes: %s", bytes, cudaGetErrorString(e));
-    layout(s, T, splits, max_tiles, mode == 2, mode != 0, static_cast<char*>(mem), &sc);
+    layout(s, T, plan, max_tiles, mode == 2, mode != 0, static_cast<char*>(mem), &sc);
     {
         int32_t* idx = mode == 0 ? topk_idx : sc.idx;
         float* w = mode == 0 ? topk_w : sc.w;
-        LAUNCH(kLogits, launch_router_logits(s, x, wr, T, splits, sc.partial, st));
-        LAUNCH(kSelect, launch_router_select(s, sc.partial, splits, mode == 1 ? nullptr : bias, T, idx, w,
+        if (plan.tensor) LAUNCH(kSplitW, launch_router_split_weights(s, wr, sc.w3, dev->num_sms, st));
+        LAUNCH(kLogits, launch_router_logits(s, plan, x, wr, T, sc.w3, sc.partial, dev->status, dev->num_sms, st));
+        LAUNCH(kSelect, launch_router_select(s, sc.partial, plan.splits, mode == 1 ? nullptr : bias, T, idx, w,
                                              mode == 1 ? logits : nullptr, st));
         if (mode == 2) {
             LAUNCH(kCount, launch_dispatch_count(s, idx, T, sc.chunk, dev->status, st));

@@ -1,27 +1,34 @@
-// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05, TMEM accumulators,
-// TMA-fed shared-memory pipeline) for the SwiGLU experts of the Beam MoE block (Glonce
-// "Reflection releases Beam ...", Architecture paragraph: each expert a SwiGLU MLP of
-// intermediate size 2,560; transformers "Beam" doc: SwiGLU activation in FP32).
+// Grouped GEMMs on the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA-fed
+// shared-memory pipeline) for the Beam MoE block: the SwiGLU experts (Glonce "Reflection
+// releases Beam ...", Architecture paragraph: each expert a SwiGLU MLP of intermediate size
+// 2,560; transformers "Beam" doc: SwiGLU activation in FP32) and the FP32 router product
+// (same doc: routing computed in FP32 with FP32 router weights).
 //
-// Both GEMMs are written "weights as M": for an N-tile of `rows` permuted token rows of
-// expert e and an M-tile of 128 weight rows,
-//     D[128 weight rows, N tokens] = W_e[m-tile, :] . X[tile rows, :]^T      (FP32, TMEM)
-// so the streamed weights are the 128-row A operand, and all of an expert's tokens (up to
-// 256) sit in the N dimension of one MMA: each weight tile is read from HBM once per
-// N-tile, which is what bounds decode and prefill.
-//   gate/up: two accumulators (gate rows, up rows) share the B tile; the epilogue computes
-//            h = silu(g) * u in FP32 and stores BF16 h[row, I].
-//   down:    one accumulator; the epilogue stores FP32 y[row, d].
+// Every mode is written "weights as M": for an N-tile of `rows` token rows and an M-tile of
+// 128 weight rows,
+//     D[128 weight rows, N tokens] = W[m-tile, :] . X[tile rows, :]^T      (FP32, TMEM)
+// so the weights are the 128-row A operand and the tile's tokens (up to kBNMax) sit in the
+// N dimension of one MMA: each weight tile is read once per N-tile.
+//   gate/up: per expert; two accumulators (gate rows, up rows) share the B tile; the
+//            epilogue computes h = silu(g) * u in FP32 and stores BF16 h[row, I].
+//   down:    per expert; one accumulator; the epilogue stores FP32 y[row, d].
+//   router:  logits = x . Wr^T with FP32 Wr given as three BF16 pieces hi + mid + lo whose
+//            sum is exactly Wr (x is exactly BF16): three MMAs per K step accumulate
+//            x.hi + x.mid + x.lo into one FP32 accumulator, i.e. the FP32 product with
+//            exact BF16 x BF16 partial products. K is split into `splits` ranges; each
+//            split stores its FP32 plane partial[split][token][expert], added in split
+//            order by the selection kernel.
 //
-// Roles (192 threads, one CTA per SM, persistent over a static round-robin of work items
-// item = n_tile * m_tiles + m_tile):
+// Roles (one CTA per SM, persistent over a static round-robin of work items):
 //   warp 0 lane 0: TMA producer - per 64-wide K chunk, the weight tile(s) [128 x 64] and
 //                  the activation rows in boxes of 16 [16 x 64], 128-byte swizzle, into a
 //                  ring of shared-memory stages (full/empty mbarriers);
 //   warp 1:        allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=rows rounded up to
 //                  16, K=16 per instruction) and tcgen05.commit to release stages and to
 //                  publish a finished accumulator;
-//   warps 2-5:     epilogue - tcgen05.ld of their 32-lane TMEM quarter, activation, stores.
+//   warps 2..:     epilogue - tcgen05.ld of their 32-lane TMEM quarter (warp % 4), the
+//                  warps of one quarter taking alternate 16-column granules; activation,
+//                  stores.
 // Accumulators are double-buffered in TMEM when two fit (512 columns), so the epilogue of
 // one tile overlaps the MMAs of the next.
 // Every mbarrier wait is bounded (2 s of wall time); on expiry the CTA records
@@ -40,18 +47,26 @@ constexpr int BM = 128;        // weight rows per tile (MMA M)
 constexpr int BK = 64;         // K per stage: one 128-byte swizzle row of BF16
 constexpr int UK = 16;         // K per tcgen05.mma (kind::f16)
 constexpr int kBoxRows = 16;   // activation rows per TMA box
-constexpr int kThreads = 192;
+#ifndef BEAM_GEMM_EPI_WARPS
+#define BEAM_GEMM_EPI_WARPS 8
+#endif
+constexpr int kEpiWarps = BEAM_GEMM_EPI_WARPS;   // warps per TMEM lane quarter = kEpiWarps / 4
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-template <bool kGateUp, int kBNMax>
+enum : int { kModeDown = 0, kModeGateUp = 1, kModeRouter = 2 };
+
+template <int kMode, int kBNMax>
 struct Cfg {
+    static constexpr int kNumA = kMode == kModeGateUp ? 2 : kMode == kModeRouter ? 3 : 1;
+    static constexpr int kNumAcc = kMode == kModeGateUp ? 2 : 1;
     static constexpr int kA = BM * BK * 2;
     static constexpr int kB = kBNMax * BK * 2;
-    static constexpr int kStage = kA * (kGateUp ? 2 : 1) + kB;
+    static constexpr int kStage = kA * kNumA + kB;
     static constexpr int kBudget = 227 * 1024 - 2048;
     static constexpr int kStages = (kBudget / kStage) > 10 ? 10 : (kBudget / kStage);
-    static constexpr int kAccCols = kBNMax * (kGateUp ? 2 : 1);
+    static constexpr int kAccCols = kBNMax * kNumAcc;
     static constexpr int kAccBufs = (2 * kAccCols <= 512) ? 2 : 1;
     static constexpr int kColsNeeded = kAccCols * kAccBufs;
     static constexpr int kTmemCols = kColsNeeded <= 32    ? 32
@@ -66,18 +81,69 @@ struct Cfg {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ void record_failure(volatile int* abort_flag, int* status) {
-    *abort_flag = 1;
-    atomicCAS(status, 0, kStatusWaitTimeout);
+// Everything the kernel needs besides the tensor maps.
+struct GemmArgs {
+    const int4* tiles;      // expert modes: header int4 (.x = tile count), then {e, row0, rows, 0}
+    int max_tiles;          // expert modes: capacity of the work list
+    int n_experts;          // expert modes: valid expert ids are [0, n_experts)
+    int total_rows;         // rows of the B operand (permuted rows, or tokens for the router)
+    int m_tiles;            // 128-row weight tiles per item column
+    int rows_per_expert;    // expert modes: A rows of one expert
+    int k_chunks;           // 64-wide K chunks per item
+    int splits;             // router: K ranges per (token tile, weight tile); else 1
+    int piece_rows;         // router: A rows between the hi, mid and lo weight pieces (E)
+    int out_cols;           // columns of the output actually stored (router: E)
+    void* out;
+    int ldo;                // output row pitch in elements
+    long long split_stride; // router: elements between the output planes of two splits
+    int* status;            // may be null
+};
+
+struct Item {
+    int4 tl;    // {expert, first B row, rows, 0}
+    int m;      // weight tile
+    int split;  // K range
+    bool ok;
+};
+
+// Decodes work item `item` the same way in every role.
+template <int kMode, int kBNMax>
+__device__ __forceinline__ Item item_of(const GemmArgs& a, int item) {
+    Item it;
+    if constexpr (kMode == kModeRouter) {
+        it.split = item % a.splits;
+        const int r = item / a.splits;
+        it.m = r % a.m_tiles;
+        const int row0 = (r / a.m_tiles) * kBNMax;
+        it.tl = make_int4(0, row0, min(kBNMax, a.total_rows - row0), 0);
+        it.ok = true;
+    } else {
+        const int4 tl = a.tiles[1 + item / a.m_tiles];
+        it.tl = tl;
+        it.m = item % a.m_tiles;
+        it.split = 0;
+        it.ok = !(tl.x < 0 || tl.x >= a.n_experts || tl.z <= 0 || tl.z > kBNMax || tl.y < 0 ||
+                  tl.y > a.total_rows - tl.z);
+    }
+    return it;
 }
 
-template <bool kGateUp, int kBNMax>
+// Records `code` in the status word unless one is already recorded (status may be null:
+// callers without a status word only get the abort behaviour).
+__device__ __forceinline__ void flag_status(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ void record_failure(volatile int* abort_flag, int* status) {
+    *abort_flag = 1;
+    flag_status(status, kStatusWaitTimeout);
+}
+
+template <int kMode, int kBNMax>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                        const __grid_constant__ CUtensorMap tmB, const int4* __restrict__ tiles, int max_tiles,
-                        int n_experts, int total_rows, int m_tiles, int rows_per_expert, int k_chunks,
-                        void* __restrict__ out, int ldo, int* status) {
-    using C = Cfg<kGateUp, kBNMax>;
+                        const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmArgs args) {
+    using C = Cfg<kMode, kBNMax>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
@@ -86,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int FULL0 = 0, EMPTY0 = C::kStages, TFULL0 = 2 * C::kStages, TEMPTY0 = TFULL0 + C::kAccBufs,
                   DRAIN = TEMPTY0 + C::kAccBufs;
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
+    int* status = args.status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -95,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < C::kAccBufs; ++b) {
             ptx::mbar_init(bar(TFULL0 + b), 1);
-            ptx::mbar_init(bar(TEMPTY0 + b), 128);
+            ptx::mbar_init(bar(TEMPTY0 + b), 32 * kEpiWarps);
         }
         ptx::mbar_init(bar(DRAIN), 1);
         *abort_flag = 0;
@@ -103,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA0);
-        if (kGateUp) ptx::prefetch_tmap(&tmA1);
+        if (kMode == kModeGateUp) ptx::prefetch_tmap(&tmA1);
         ptx::prefetch_tmap(&tmB);
     }
     if (warp == 1) {
@@ -114,48 +181,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    int n_tiles = tiles[0].x;
-    if (n_tiles < 0 || n_tiles > max_tiles) {
-        if (threadIdx.x == 0) atomicCAS(status, 0, kStatusBadIndex);
-        n_tiles = 0;
+    int n_items;
+    if constexpr (kMode == kModeRouter) {
+        n_items = ((args.total_rows + kBNMax - 1) / kBNMax) * args.m_tiles * args.splits;
+    } else {
+        int n_tiles = args.tiles[0].x;
+        if (n_tiles < 0 || n_tiles > args.max_tiles) {
+            if (threadIdx.x == 0) flag_status(status, kStatusBadIndex);
+            n_tiles = 0;
+        }
+        n_items = n_tiles * args.m_tiles;
     }
-    const int n_items = n_tiles * m_tiles;
-    // A work-list entry every role checks the same way; a bad one is skipped by all roles.
-    auto bad_tile = [&](const int4& tl) {
-        return tl.x < 0 || tl.x >= n_experts || tl.z <= 0 || tl.z > kBNMax || tl.y < 0 || tl.y > total_rows - tl.z;
-    };
+    const int k_chunks = args.k_chunks;
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producer
-            const uint64_t pol_w = ptx::policy_evict_first();
+            // Expert weights stream once (evict first); the router's weight pieces are
+            // re-read by every token tile (keep them).
+            const uint64_t pol_w = kMode == kModeRouter ? ptx::policy_evict_last() : ptx::policy_evict_first();
             const uint64_t pol_x = ptx::policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, parity = 0;  // per stage: ever loaded / parity of the last load
             bool ok = true;
             for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-                const int4 tl = tiles[1 + item / m_tiles];
-                const int m = item % m_tiles;
-                if (bad_tile(tl)) {
-                    atomicCAS(status, 0, kStatusBadIndex);
+                const Item it = item_of<kMode, kBNMax>(args, item);
+                if (!it.ok) {
+                    flag_status(status, kStatusBadIndex);
                     continue;
                 }
-                const int nbox = (tl.z + kBoxRows - 1) / kBoxRows;
-                const uint32_t bytes = C::kA * (kGateUp ? 2 : 1) + nbox * kBoxRows * BK * 2;
-                const int a_row = tl.x * rows_per_expert + m * BM;
+                const int nbox = (it.tl.z + kBoxRows - 1) / kBoxRows;
+                const uint32_t bytes = C::kA * C::kNumA + nbox * kBoxRows * BK * 2;
+                const int a_row = (kMode == kModeRouter ? 0 : it.tl.x * args.rows_per_expert) + it.m * BM;
+                const int kc0 = it.split * k_chunks;
                 for (int kc = 0; kc < k_chunks; ++kc) {
+                    const int kx = (kc0 + kc) * BK;
                     if (!ptx::mbar_wait(bar(EMPTY0 + stage), phase ^ 1, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     const uint32_t sa = ptx::smem_u32(smem + stage * C::kStage);
                     ptx::mbar_arrive_expect_tx(bar(FULL0 + stage), bytes);
-                    ptx::tma_load_2d(sa, &tmA0, kc * BK, a_row, bar(FULL0 + stage), pol_w);
-                    if (kGateUp) ptx::tma_load_2d(sa + C::kA, &tmA1, kc * BK, a_row, bar(FULL0 + stage), pol_w);
-                    const uint32_t sb = sa + C::kA * (kGateUp ? 2 : 1);
+#pragma unroll
+                    for (int j = 0; j < C::kNumA; ++j) {
+                        const CUtensorMap* map = (kMode == kModeGateUp && j == 1) ? &tmA1 : &tmA0;
+                        const int row = a_row + (kMode == kModeRouter ? j * args.piece_rows : 0);
+                        ptx::tma_load_2d(sa + j * C::kA, map, kx, row, bar(FULL0 + stage), pol_w);
+                    }
+                    const uint32_t sb = sa + C::kA * C::kNumA;
                     for (int j = 0; j < nbox; ++j)
-                        ptx::tma_load_2d(sb + j * kBoxRows * BK * 2, &tmB, kc * BK, tl.y + j * kBoxRows,
+                        ptx::tma_load_2d(sb + j * kBoxRows * BK * 2, &tmB, kx, it.tl.y + j * kBoxRows,
                                          bar(FULL0 + stage), pol_x);
                     issued |= 1u << stage;
                     parity = (parity & ~(1u << stage)) | (phase << stage);
@@ -179,9 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-                const int4 tl = tiles[1 + item / m_tiles];
-                if (bad_tile(tl)) continue;
-                const int n_mma = ((tl.z + 15) / 16) * 16;
+                const Item it = item_of<kMode, kBNMax>(args, item);
+                if (!it.ok) continue;
+                const int n_mma = ((it.tl.z + 15) / 16) * 16;
                 const uint32_t idesc = ptx::idesc_bf16_f32(BM, n_mma);
                 if (!ptx::mbar_wait(bar(TEMPTY0 + acc), acc_phase ^ 1, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -196,15 +272,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_u32(smem + stage * C::kStage);
-                    const uint32_t sb = sa + C::kA * (kGateUp ? 2 : 1);
+                    const uint32_t sb = sa + C::kA * C::kNumA;
 #pragma unroll
                     for (int kk = 0; kk < BK / UK; ++kk) {
                         const uint64_t bdesc = ptx::sw128_kmajor_desc(sb + kk * UK * 2);
-                        const uint32_t accum = (kc | kk) ? 1u : 0u;
-                        ptx::mma_bf16(d0, ptx::sw128_kmajor_desc(sa + kk * UK * 2), bdesc, idesc, accum);
-                        if (kGateUp)
-                            ptx::mma_bf16(d0 + kBNMax, ptx::sw128_kmajor_desc(sa + C::kA + kk * UK * 2), bdesc, idesc,
-                                          accum);
+                        if constexpr (kMode == kModeRouter) {
+#pragma unroll
+                            for (int j = 0; j < C::kNumA; ++j)
+                                ptx::mma_bf16(d0, ptx::sw128_kmajor_desc(sa + j * C::kA + kk * UK * 2), bdesc, idesc,
+                                              (kc | kk | j) ? 1u : 0u);
+                        } else {
+                            const uint32_t accum = (kc | kk) ? 1u : 0u;
+                            ptx::mma_bf16(d0, ptx::sw128_kmajor_desc(sa + kk * UK * 2), bdesc, idesc, accum);
+                            if (kMode == kModeGateUp)
+                                ptx::mma_bf16(d0 + kBNMax, ptx::sw128_kmajor_desc(sa + C::kA + kk * UK * 2), bdesc,
+                                              idesc, accum);
+                        }
                     }
                     ptx::mma_commit(bar(EMPTY0 + stage));
                     if (++stage == C::kStages) {
@@ -228,44 +311,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- epilogue
-        const int q = warp & 3;           // TMEM lane quarter this warp may access
-        const int row = q * 32 + lane;    // weight row within the M-tile
+        const int q = warp & 3;                          // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;                   // weight row within the M-tile
+        const int col_part = (warp - 2) >> 2;            // which 16-column granules this warp takes
+        constexpr int kColStep = 16 * (kEpiWarps / 4);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-            const int4 tl = tiles[1 + item / m_tiles];
-            const int m = item % m_tiles;
-            if (bad_tile(tl)) continue;
+            const Item it = item_of<kMode, kBNMax>(args, item);
+            if (!it.ok) continue;
             if (!ptx::mbar_wait(bar(TFULL0 + acc), acc_phase, abort_flag, kWaitLimitNs)) {
                 record_failure(abort_flag, status);
                 break;
             }
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
-            const size_t col = static_cast<size_t>(m) * BM + row;
-            for (int c0 = 0; c0 < tl.z; c0 += 16) {
+            const int col = it.m * BM + row;
+            const bool col_ok = col < args.out_cols;
+            for (int c0 = col_part * 16; c0 < it.tl.z; c0 += kColStep) {
                 uint32_t g[16];
                 ptx::tmem_ld16(taddr + c0, g);
-                if constexpr (kGateUp) {
+                if constexpr (kMode == kModeGateUp) {
                     uint32_t u[16];
                     ptx::tmem_ld16(taddr + kBNMax + c0, u);
                     ptx::tmem_wait_ld();
-                    bf16* h = static_cast<bf16*>(out);
+                    bf16* h = static_cast<bf16*>(args.out);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        if (c0 + j < tl.z) {
+                        if (c0 + j < it.tl.z && col_ok) {
                             const float gv = __uint_as_float(g[j]);
                             const float uv = __uint_as_float(u[j]);
                             const float hv = gv / (1.0f + expf(-gv)) * uv;
-                            h[static_cast<size_t>(tl.y + c0 + j) * ldo + col] = __float2bfloat16_rn(hv);
+                            h[static_cast<size_t>(it.tl.y + c0 + j) * args.ldo + col] = __float2bfloat16_rn(hv);
                         }
                     }
                 } else {
                     ptx::tmem_wait_ld();
-                    float* y = static_cast<float*>(out);
+                    float* y = static_cast<float*>(args.out) + it.split * args.split_stride;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < tl.z) y[static_cast<size_t>(tl.y + c0 + j) * ldo + col] = __uint_as_float(g[j]);
+                        if (c0 + j < it.tl.z && col_ok)
+                            y[static_cast<size_t>(it.tl.y + c0 + j) * args.ldo + col] = __uint_as_float(g[j]);
                 }
             }
             ptx::tc_fence_before();
@@ -286,16 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool kGateUp, int kBNMax>
-cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const int4* tiles,
-                        int max_tiles, int n_experts, int total_rows, int m_tiles, int rows_per_expert, int k_chunks,
-                        void* out, int ldo, int* status, int grid, cudaStream_t st) {
-    using C = Cfg<kGateUp, kBNMax>;
-    auto kern = grouped_gemm_kernel<kGateUp, kBNMax>;
+template <int kMode, int kBNMax>
+cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const GemmArgs& args,
+                        int grid, cudaStream_t st) {
+    using C = Cfg<kMode, kBNMax>;
+    auto kern = grouped_gemm_kernel<kMode, kBNMax>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, C::kSmemBytes, st>>>(a0, a1, b, tiles, max_tiles, n_experts, total_rows, m_tiles,
-                                                rows_per_expert, k_chunks, out, ldo, status);
+    kern<<<grid, kThreads, C::kSmemBytes, st>>>(a0, a1, b, args);
     return cudaGetLastError();
 }
 
@@ -317,10 +401,32 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-int grid_for(int max_items, int num_sms) {
-    int g = max_items < num_sms ? max_items : num_sms;
-    return g < 1 ? 1 : g;
+int grid_for(long long max_items, int num_sms) {
+    long long g = max_items < num_sms ? max_items : num_sms;
+    return g < 1 ? 1 : static_cast<int>(g);
 }
+
+GemmArgs expert_args(const int4* tiles, int max_tiles, int n_experts, int rows, int m_tiles, int rows_per_expert,
+                     int k_chunks, void* out, int ldo, int* status) {
+    GemmArgs a;
+    a.tiles = tiles;
+    a.max_tiles = max_tiles;
+    a.n_experts = n_experts;
+    a.total_rows = rows;
+    a.m_tiles = m_tiles;
+    a.rows_per_expert = rows_per_expert;
+    a.k_chunks = k_chunks;
+    a.splits = 1;
+    a.piece_rows = 0;
+    a.out_cols = m_tiles * BM;
+    a.out = out;
+    a.ldo = ldo;
+    a.split_stride = 0;
+    a.status = status;
+    return a;
+}
+
+constexpr int kRouterBN = 128;  // tokens per router N-tile
 
 }  // namespace
 
@@ -345,7 +451,10 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint
     return true;
 }
 
-int gemm_bn_max(int T) { return T <= 32 ? 32 : 256; }
+#ifndef BEAM_GEMM_BN128_MAX_T
+#define BEAM_GEMM_BN128_MAX_T 0
+#endif
+int gemm_bn_max(int T) { return T <= 32 ? 32 : T <= BEAM_GEMM_BN128_MAX_T ? 128 : 256; }
 
 cudaError_t launch_gateup(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* x_perm, int rows,
                           const int4* tiles, int max_tiles, int bn_max, bf16* h, int* status, int num_sms,
@@ -357,12 +466,11 @@ cudaError_t launch_gateup(const Shape& s, const bf16* w_gate, const bf16* w_up, 
         !encode_tmap_bf16_2d(&b, x_perm, rows, s.d, kBoxRows, BK, &why))
         return cudaErrorInvalidValue;
     const int m_tiles = s.I / BM;
-    const int grid = grid_for(max_tiles * m_tiles, num_sms);
-    if (bn_max <= 32)
-        return launch_gemm<true, 32>(a0, a1, b, tiles, max_tiles, s.E, rows, m_tiles, s.I, s.d / BK, h, s.I, status,
-                                     grid, st);
-    return launch_gemm<true, 256>(a0, a1, b, tiles, max_tiles, s.E, rows, m_tiles, s.I, s.d / BK, h, s.I, status,
-                                  grid, st);
+    const GemmArgs args = expert_args(tiles, max_tiles, s.E, rows, m_tiles, s.I, s.d / BK, h, s.I, status);
+    const int grid = grid_for(static_cast<long long>(max_tiles) * m_tiles, num_sms);
+    if (bn_max <= 32) return launch_gemm<kModeGateUp, 32>(a0, a1, b, args, grid, st);
+    if (bn_max <= 128) return launch_gemm<kModeGateUp, 128>(a0, a1, b, args, grid, st);
+    return launch_gemm<kModeGateUp, 256>(a0, a1, b, args, grid, st);
 }
 
 cudaError_t launch_down(const Shape& s, const bf16* w_down, const bf16* h, int rows, const int4* tiles, int max_tiles,
@@ -373,12 +481,51 @@ cudaError_t launch_down(const Shape& s, const bf16* w_down, const bf16* h, int r
         !encode_tmap_bf16_2d(&b, h, rows, s.I, kBoxRows, BK, &why))
         return cudaErrorInvalidValue;
     const int m_tiles = s.d / BM;
-    const int grid = grid_for(max_tiles * m_tiles, num_sms);
-    if (bn_max <= 32)
-        return launch_gemm<false, 32>(a0, a0, b, tiles, max_tiles, s.E, rows, m_tiles, s.d, s.I / BK, y, s.d, status,
-                                      grid, st);
-    return launch_gemm<false, 256>(a0, a0, b, tiles, max_tiles, s.E, rows, m_tiles, s.d, s.I / BK, y, s.d, status,
-                                   grid, st);
+    const GemmArgs args = expert_args(tiles, max_tiles, s.E, rows, m_tiles, s.d, s.I / BK, y, s.d, status);
+    const int grid = grid_for(static_cast<long long>(max_tiles) * m_tiles, num_sms);
+    if (bn_max <= 32) return launch_gemm<kModeDown, 32>(a0, a0, b, args, grid, st);
+    if (bn_max <= 128) return launch_gemm<kModeDown, 128>(a0, a0, b, args, grid, st);
+    return launch_gemm<kModeDown, 256>(a0, a0, b, args, grid, st);
+}
+
+int router_tc_splits(const Shape& s, int T, int num_sms) {
+    // Estimated time on the busiest SM, in ns: ~550 per K chunk of an item and ~1500 per
+    // item (pipeline fill, epilogue), plus the partial planes written here and read back by
+    // the selection kernel at ~6 TB/s. Ties go to fewer splits.
+    const int kc_total = s.d / BK;
+    const long long tiles = static_cast<long long>((T + kRouterBN - 1) / kRouterBN) * ((s.E + BM - 1) / BM);
+    int best = 1;
+    long long best_cost = -1;
+    for (int sp = 1; sp <= 16 && sp <= kc_total; ++sp) {
+        if (kc_total % sp) continue;
+        const long long items = tiles * sp;
+        const long long waves = (items + num_sms - 1) / num_sms;
+        const long long cost = waves * ((kc_total / sp) * 550ll + 1500ll) +
+                               static_cast<long long>(sp) * T * s.E * 8 / 6000;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = sp;
+        }
+    }
+    return best;
+}
+
+cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int T, int splits, float* partial,
+                             int* status, int num_sms, cudaStream_t st) {
+    CUtensorMap a0, b;
+    const char* why = nullptr;
+    if (!encode_tmap_bf16_2d(&a0, w3, 3ull * s.E, s.d, BM, BK, &why) ||
+        !encode_tmap_bf16_2d(&b, x, T, s.d, kBoxRows, BK, &why))
+        return cudaErrorInvalidValue;
+    const int kc_total = s.d / BK;
+    if (splits < 1 || kc_total % splits) return cudaErrorInvalidValue;
+    GemmArgs a = expert_args(nullptr, 0, 1, T, (s.E + BM - 1) / BM, 0, kc_total / splits, partial, s.E, status);
+    a.splits = splits;
+    a.piece_rows = s.E;
+    a.out_cols = s.E;
+    a.split_stride = static_cast<long long>(T) * s.E;
+    const long long items = static_cast<long long>((T + kRouterBN - 1) / kRouterBN) * a.m_tiles * splits;
+    return launch_gemm<kModeRouter, kRouterBN>(a0, a0, b, a, grid_for(items, num_sms), st);
 }
 
 }  // namespace beam

@@ -25,9 +25,19 @@ enum : int { kStatusOk = 0, kStatusBadExpert = 1, kStatusWaitTimeout = 2, kStatu
 constexpr int kDispatchChunk = 256;  // tokens per dispatch block
 
 // ---------------------------------------------------------------- router (router.cu)
-int router_splits(const Shape& s, int T, int num_sms);
-cudaError_t launch_router_logits(const Shape& s, const bf16* x, const float* wr, int T, int splits, float* partial,
-                                 cudaStream_t st);
+// How the router's logits stage runs for T tokens: the small-batch CUDA-core kernel
+// (T <= 32, one partial plane) or the tensor-core product over BF16 pieces of the FP32
+// router weights (split-K partial planes).
+struct RouterPlan {
+    bool tensor;      // tensor-core path (needs the weight pieces)
+    int splits;       // partial planes of [T, E] the logits stage writes
+    size_t w3_elems;  // BF16 elements of the three weight pieces (0 on the CUDA-core path)
+};
+RouterPlan router_plan(const Shape& s, int T, int num_sms);
+// Writes the pieces hi, mid, lo of router_w ([3][E][d] BF16) for the tensor-core path.
+cudaError_t launch_router_split_weights(const Shape& s, const float* wr, bf16* w3, int num_sms, cudaStream_t st);
+cudaError_t launch_router_logits(const Shape& s, const RouterPlan& p, const bf16* x, const float* wr, int T,
+                                 const bf16* w3, float* partial, int* status, int num_sms, cudaStream_t st);
 cudaError_t launch_router_select(const Shape& s, const float* partial, int splits, const float* bias, int T,
                                  int32_t* topk_idx, float* topk_w, float* logits_out, cudaStream_t st);
 
@@ -49,6 +59,11 @@ int gemm_bn_max(int T);
 cudaError_t launch_gateup(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* x_perm, int rows,
                           const int4* tiles, int max_tiles, int bn_max, bf16* h, int* status, int num_sms,
                           cudaStream_t st);
+// Split-K count of the tensor-core router product for T tokens.
+int router_tc_splits(const Shape& s, int T, int num_sms);
+// partial[split][t][e] = sum over the split's K range of x[t] . (hi + mid + lo)[e].
+cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int T, int splits, float* partial,
+                             int* status, int num_sms, cudaStream_t st);
 // y[rows, d] = h . Wd[e]^T (FP32), per N-tile of the work list.
 cudaError_t launch_down(const Shape& s, const bf16* w_down, const bf16* h, int rows, const int4* tiles, int max_tiles,
                         int bn_max, float* y, int* status, int num_sms, cudaStream_t st);

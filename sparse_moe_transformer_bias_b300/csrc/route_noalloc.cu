@@ -6,15 +6,16 @@
 // that: a serving engine that has already claimed all free HBM for its weights and KV
 // cache (an allocation would fail), or a runtime that allows no allocator call on its
 // per-token path, where a new allocation may synchronise the device or add unbounded
-// latency. This entry point gives them the router with its only scratch buffer (the
-// split-K partial logits) in a fixed array that is part of the library's device image.
+// latency. This entry point gives them the router with its scratch (the BF16 pieces of
+// the router weights and the split-K partial logits) in a fixed array that is part of the
+// library's device image.
 //
-// The array: BEAM_MOE_NOALLOC_SCRATCH_BYTES (16 MiB). It is created when the library's
+// The array: BEAM_MOE_NOALLOC_SCRATCH_BYTES (40 MiB). It is created when the library's
 // device code is loaded on a GPU, and that GPU keeps it until the process exits, whether
-// or not this entry point is ever called. It fits the partial logits of any call with
-// T <= BEAM_MOE_NOALLOC_MAX_TOKENS (8192). On a GPU whose SM count would make the router
-// pick more K splits than the array holds, fewer splits are used; only the summation
-// order of the logits changes then.
+// or not this entry point is ever called. It fits the router scratch of any call with
+// T <= BEAM_MOE_NOALLOC_MAX_TOKENS (8192) at Beam's shape on GPUs of up to ~170 SMs. On a
+// GPU where the router would pick more K splits than the array holds, fewer splits are
+// used; only the summation order of the logits changes then.
 //
 // Host code cannot pass the array's name to a kernel (on the host it is a stand-in
 // symbol, not a device address), so the first call on each device looks up the array's
@@ -29,7 +30,7 @@
 
 #include "internal.cuh"
 
-static __device__ __align__(256) float g_route_noalloc_scratch[BEAM_MOE_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+static __device__ __align__(256) uint8_t g_route_noalloc_scratch[BEAM_MOE_NOALLOC_SCRATCH_BYTES];
 
 namespace beam {
 namespace {
@@ -37,7 +38,7 @@ namespace {
 struct NoAllocDevice {
     bool ready = false;
     int num_sms = 0;
-    float* scratch = nullptr;  // device address of g_route_noalloc_scratch on this device
+    uint8_t* scratch = nullptr;  // device address of g_route_noalloc_scratch on this device
 };
 constexpr int kMaxNoAllocDevices = 64;
 NoAllocDevice g_noalloc[kMaxNoAllocDevices];
@@ -57,7 +58,7 @@ int noalloc_device(NoAllocDevice** out) {
         void* p = nullptr;
         if ((e = cudaGetSymbolAddress(&p, g_route_noalloc_scratch)) != cudaSuccess || p == nullptr)
             return abi_fail(BEAM_MOE_ERR_CUDA, "cudaGetSymbolAddress(router scratch): %s", cudaGetErrorString(e));
-        s.scratch = static_cast<float*>(p);
+        s.scratch = static_cast<uint8_t*>(p);
         s.ready = true;
     }
     *out = &s;
@@ -89,17 +90,30 @@ extern "C" int beam_moe_route_noalloc(const beam_moe_config* cfg, const __nv_bfl
     if ((rc = noalloc_device(&dev))) return rc;
 
     const Shape s{cfg->d, cfg->I, cfg->E, cfg->n_group, cfg->topk_group, cfg->top_k, cfg->scale};
-    const size_t capacity = sizeof(g_route_noalloc_scratch) / sizeof(float);
-    const int nk = s.d / 32;  // K steps of the logits kernel; splits divide it
-    int splits = router_splits(s, T, dev->num_sms);
-    while (splits > 1 && static_cast<size_t>(splits) * T * s.E > capacity) {
+    // Same plan as beam_moe_route_ex; layout: weight pieces, then the partial planes.
+    RouterPlan plan = router_plan(s, T, dev->num_sms);
+    const size_t w3_bytes = (plan.w3_elems * sizeof(bf16) + 255) & ~size_t(255);
+    const size_t capacity = sizeof(g_route_noalloc_scratch);
+    const int nk = s.d / 64;  // K chunks of the tensor-core product; its splits divide it
+    while (plan.splits > 1 && w3_bytes + static_cast<size_t>(plan.splits) * T * s.E * sizeof(float) > capacity) {
         do {
-            --splits;
-        } while (nk % splits);
+            --plan.splits;
+        } while (nk % plan.splits);
     }
-    cudaError_t e = launch_router_logits(s, x, router_w, T, splits, dev->scratch, stream);
+    if (w3_bytes + static_cast<size_t>(plan.splits) * T * s.E * sizeof(float) > capacity)
+        return abi_fail(BEAM_MOE_ERR_ARG, "T=%d with E=%d and d=%d needs more router scratch than the %u bytes of "
+                        "beam_moe_route_noalloc", T, s.E, s.d, static_cast<unsigned>(capacity));
+    bf16* w3 = plan.tensor ? reinterpret_cast<bf16*>(dev->scratch) : nullptr;
+    float* partial = reinterpret_cast<float*>(dev->scratch + w3_bytes);
+    cudaError_t e = cudaSuccess;
+    if (plan.tensor) {
+        e = launch_router_split_weights(s, router_w, w3, dev->num_sms, stream);
+        if (e != cudaSuccess)
+            return abi_fail(BEAM_MOE_ERR_CUDA, "launch of router weight split failed: %s", cudaGetErrorString(e));
+    }
+    e = launch_router_logits(s, plan, x, router_w, T, w3, partial, nullptr, dev->num_sms, stream);
     if (e != cudaSuccess) return abi_fail(BEAM_MOE_ERR_CUDA, "launch of router logits failed: %s", cudaGetErrorString(e));
-    e = launch_router_select(s, dev->scratch, splits, expert_bias, T, topk_idx, topk_w, nullptr, stream);
+    e = launch_router_select(s, partial, plan.splits, expert_bias, T, topk_idx, topk_w, nullptr, stream);
     if (e != cudaSuccess) return abi_fail(BEAM_MOE_ERR_CUDA, "launch of router select failed: %s", cudaGetErrorString(e));
     return BEAM_MOE_OK;
 }

@@ -2,10 +2,13 @@
 // Architecture paragraph; transformers "Beam" doc, Overview, "Sparse MoE" bullet and the
 // FP32-numerics paragraph after the bullets).
 //
-// Stage 1 (router_logits_kernel): FP32 logits l = x . Wr^T on CUDA cores, x widened
-// exactly from BF16, FP32 fused multiply-adds in ascending K order. Split-K partial sums
-// (for small T) are written per split and added in split order by stage 2, so the result
-// is deterministic.
+// Stage 1: FP32 logits l = x . Wr^T (x is exactly BF16).
+//   T <= 32 (decode): router_logits_small_kernel on CUDA cores, FP32 fused multiply-adds,
+//   one CTA per two experts over the whole K, reduced in a fixed order.
+//   T > 32: the tensor-core product of grouped_gemm.cu in router mode, after
+//   router_split_weights_kernel has written Wr as three BF16 pieces hi + mid + lo == Wr
+//   (exactly); the products x.piece are exact and accumulate in FP32. Split-K partial
+//   planes are added in split order by stage 2, so the result is deterministic.
 // Stage 2 (router_select_kernel): one warp per token. Lane j holds expert 32g + j of every
 // group g in registers: sigmoid, bias add, group top-2 sums by butterfly shuffles, group
 // top-k and expert top-k by warp argmax rounds, weights normalised to `scale`.
@@ -17,93 +20,76 @@
 namespace beam {
 namespace {
 
-constexpr int RT = 64;    // tokens per CTA
-constexpr int RE = 64;    // experts per CTA
-constexpr int RK = 32;    // K per shared-memory stage
-constexpr int RTHREADS = 256;
+constexpr unsigned kFull = 0xffffffffu;
 
-__global__ void __launch_bounds__(RTHREADS) router_logits_kernel(const bf16* __restrict__ x,
-                                                                 const float* __restrict__ wr, int T, int d, int E,
-                                                                 int k_per_split, float* __restrict__ partial) {
-    __shared__ __align__(16) float xs[2][RK][RT + 4];
-    __shared__ __align__(16) float ws[2][RK][RE + 4];
-    const int tid = threadIdx.x;
-    const int t0 = blockIdx.x * RT, e0 = blockIdx.y * RE, split = blockIdx.z;
-    const int kbeg = split * k_per_split, kend = kbeg + k_per_split;
+// Small batches (T <= kSmallT, decode): one CTA per kSmallEPB experts computes their logits
+// for every token over the whole K, so no split-K partials are written. Warp w sums the
+// K range [w*d/8, (w+1)*d/8) with lane-strided 4-wide FMAs in ascending K; the 32 lanes
+// are combined by a fixed butterfly and the 8 warps in warp order, so the result is
+// deterministic.
+constexpr int kSmallT = 32;
+constexpr int kSmallEPB = 2;
+constexpr int kSmallWarps = 8;
 
-    // Global->shared mapping: x row xt, 8 bf16 at xk; W rows we and we+32, 4 floats at wk.
-    const int xt = tid >> 2, xk = (tid & 3) * 8;
-    const int we = tid >> 3, wk = (tid & 7) * 4;
-    const bool x_ok = (t0 + xt) < T;
-    const bool w0_ok = (e0 + we) < E, w1_ok = (e0 + we + 32) < E;
-    const bf16* xp = x + static_cast<size_t>(x_ok ? t0 + xt : 0) * d + xk;
-    const float* wp0 = wr + static_cast<size_t>(w0_ok ? e0 + we : 0) * d + wk;
-    const float* wp1 = wr + static_cast<size_t>(w1_ok ? e0 + we + 32 : 0) * d + wk;
-
-    // Compute mapping: tokens ty*4..ty*4+3, experts tx*4..tx*4+3.
-    const int tx = tid & 15, ty = tid >> 4;
-    float acc[4][4];
+__global__ void __launch_bounds__(kSmallWarps * 32) router_logits_small_kernel(const bf16* __restrict__ x,
+                                                                              const float* __restrict__ wr, int T,
+                                                                              int d, int E,
+                                                                              float* __restrict__ logits) {
+    __shared__ float red[kSmallWarps][kSmallT * kSmallEPB];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * kSmallEPB;
+    const int kw = d / kSmallWarps;
+    const int kbeg = warp * kw, kend = kbeg + kw;
+    float acc[kSmallT][kSmallEPB];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int t = 0; t < kSmallT; ++t)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-    uint4 xr;
-    float4 w0r, w1r;
-    auto gload = [&](int k) {
-        xr = x_ok ? *reinterpret_cast<const uint4*>(xp + k) : make_uint4(0, 0, 0, 0);
-        w0r = w0_ok ? *reinterpret_cast<const float4*>(wp0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-        w1r = w1_ok ? *reinterpret_cast<const float4*>(wp1 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-    };
-    auto sstore = [&](int b) {
-        const bf16* xv = reinterpret_cast<const bf16*>(&xr);
+        for (int j = 0; j < kSmallEPB; ++j) acc[t][j] = 0.f;
+    for (int k = kbeg + 4 * lane; k < kend; k += 128) {
+        float4 w[kSmallEPB];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xs[b][xk + i][xt] = __bfloat162float(xv[i]);
-        ws[b][wk + 0][we] = w0r.x;
-        ws[b][wk + 1][we] = w0r.y;
-        ws[b][wk + 2][we] = w0r.z;
-        ws[b][wk + 3][we] = w0r.w;
-        ws[b][wk + 0][we + 32] = w1r.x;
-        ws[b][wk + 1][we + 32] = w1r.y;
-        ws[b][wk + 2][we + 32] = w1r.z;
-        ws[b][wk + 3][we + 32] = w1r.w;
-    };
-
-    gload(kbeg);
-    sstore(0);
-    __syncthreads();
-    int b = 0;
-    for (int k = kbeg; k < kend; k += RK) {
-        const bool more = k + RK < kend;
-        if (more) gload(k + RK);
+        for (int j = 0; j < kSmallEPB; ++j)
+            w[j] = (e0 + j < E) ? *reinterpret_cast<const float4*>(wr + static_cast<size_t>(e0 + j) * d + k)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int kk = 0; kk < RK; ++kk) {
-            const float4 a = *reinterpret_cast<const float4*>(&xs[b][kk][ty * 4]);
-            const float4 w = *reinterpret_cast<const float4*>(&ws[b][kk][tx * 4]);
-            const float av[4] = {a.x, a.y, a.z, a.w};
-            const float wv[4] = {w.x, w.y, w.z, w.w};
+        for (int t = 0; t < kSmallT; ++t) {
+            if (t < T) {
+                const uint2 raw = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * d + k);
+                const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+                const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+                const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], wv[j], acc[i][j]);
+                for (int j = 0; j < kSmallEPB; ++j) {
+                    float v = acc[t][j];
+                    v = fmaf(a.x, w[j].x, v);
+                    v = fmaf(a.y, w[j].y, v);
+                    v = fmaf(b.x, w[j].z, v);
+                    v = fmaf(b.y, w[j].w, v);
+                    acc[t][j] = v;
+                }
+            }
         }
-        if (more) sstore(b ^ 1);
-        __syncthreads();
-        b ^= 1;
     }
-    const int e = e0 + tx * 4;
-    if (e < E) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = t0 + ty * 4 + i;
-            if (t < T)
-                *reinterpret_cast<float4*>(partial + (static_cast<size_t>(split) * T + t) * E + e) =
-                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    for (int t = 0; t < kSmallT; ++t) {
+#pragma unroll
+        for (int j = 0; j < kSmallEPB; ++j) {
+            float v = acc[t][j];
+#pragma unroll
+            for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+            if (lane == 0) red[warp][t * kSmallEPB + j] = v;
         }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < T * kSmallEPB; i += blockDim.x) {
+        const int t = i / kSmallEPB, j = i % kSmallEPB;
+        if (e0 + j >= E) continue;
+        float v = red[0][i];
+#pragma unroll
+        for (int w = 1; w < kSmallWarps; ++w) v += red[w][i];
+        logits[static_cast<size_t>(t) * E + e0 + j] = v;
     }
 }
-
-constexpr unsigned kFull = 0xffffffffu;
 
 // One warp per token. Experts per group are 32 (one per lane); up to 8 groups. `bias` may
 // be null (logits-only calls), in which case the biased score is the sigmoid score.
@@ -207,25 +193,68 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
     }
 }
 
-}  // namespace
-
-int router_splits(const Shape& s, int T, int num_sms) {
-    const int nk = s.d / RK;
-    const int base = ((T + RT - 1) / RT) * ((s.E + RE - 1) / RE);
-    int best = 1;
-    for (int sp = 1; sp <= 32 && sp <= nk; ++sp) {
-        if (nk % sp) continue;
-        best = sp;
-        if (base * sp >= 2 * num_sms) break;
+// FP32 router weights as three BF16 pieces with hi + mid + lo == w exactly: hi is w
+// rounded to BF16, mid the rounded remainder, lo the rest. Each remainder is exact in FP32
+// (the difference of two numbers within a factor of two), and the last one has at most 8
+// significant bits, so it is a BF16 value (for |w| above the BF16 normal range's bottom
+// plus 16 binades, far below any router weight).
+__global__ void __launch_bounds__(256) router_split_weights_kernel(const float4* __restrict__ w, size_t n4,
+                                                                  size_t n, bf16* __restrict__ w3) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const float4 v = w[i];
+        const float vs[4] = {v.x, v.y, v.z, v.w};
+        bf16 hi[4], mid[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            hi[j] = __float2bfloat16_rn(vs[j]);
+            const float r1 = vs[j] - __bfloat162float(hi[j]);
+            mid[j] = __float2bfloat16_rn(r1);
+            const float r2 = r1 - __bfloat162float(mid[j]);
+            lo[j] = __float2bfloat16_rn(r2);
+        }
+        *reinterpret_cast<uint2*>(w3 + 4 * i) = *reinterpret_cast<const uint2*>(hi);
+        *reinterpret_cast<uint2*>(w3 + n + 4 * i) = *reinterpret_cast<const uint2*>(mid);
+        *reinterpret_cast<uint2*>(w3 + 2 * n + 4 * i) = *reinterpret_cast<const uint2*>(lo);
     }
-    return best;
 }
 
-cudaError_t launch_router_logits(const Shape& s, const bf16* x, const float* wr, int T, int splits, float* partial,
-                                 cudaStream_t st) {
-    const dim3 grid((T + RT - 1) / RT, (s.E + RE - 1) / RE, splits);
-    router_logits_kernel<<<grid, RTHREADS, 0, st>>>(x, wr, T, s.d, s.E, s.d / splits, partial);
+}  // namespace
+
+RouterPlan router_plan(const Shape& s, int T, int num_sms) {
+    RouterPlan p;
+    if (T <= kSmallT) {
+        p.tensor = false;
+        p.splits = 1;
+        p.w3_elems = 0;
+    } else {
+        p.tensor = true;
+        p.splits = router_tc_splits(s, T, num_sms);
+        p.w3_elems = 3ull * s.E * s.d;
+    }
+    return p;
+}
+
+cudaError_t launch_router_split_weights(const Shape& s, const float* wr, bf16* w3, int num_sms, cudaStream_t st) {
+    const size_t n = static_cast<size_t>(s.E) * s.d;
+    const size_t n4 = n / 4;
+    long long blocks = static_cast<long long>((n4 + 255) / 256);
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    router_split_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const float4*>(wr),
+                                                                               n4, n, w3);
     return cudaGetLastError();
+}
+
+cudaError_t launch_router_logits(const Shape& s, const RouterPlan& p, const bf16* x, const float* wr, int T,
+                                 const bf16* w3, float* partial, int* status, int num_sms, cudaStream_t st) {
+    if (!p.tensor) {
+        if (p.splits != 1 || T > kSmallT) return cudaErrorInvalidValue;
+        router_logits_small_kernel<<<(s.E + kSmallEPB - 1) / kSmallEPB, kSmallWarps * 32, 0, st>>>(x, wr, T, s.d, s.E,
+                                                                                                partial);
+        return cudaGetLastError();
+    }
+    return launch_router_tc(s, w3, x, T, p.splits, partial, status, num_sms, st);
 }
 
 cudaError_t launch_router_select(const Shape& s, const float* partial, int splits, const float* bias, int T,

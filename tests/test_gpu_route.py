@@ -30,6 +30,21 @@ def test_tiny_route_parity(T):
     assert len(flagged) <= max(2, T // 100), f"{len(flagged)} near-tie tokens"
 
 
+@pytest.mark.parametrize("n_group,d,T", [(3, 256, 300), (5, 384, 33), (1, 128, 1000), (8, 512, 4097), (2, 128, 32)])
+def test_odd_shape_route_parity(n_group, d, T):
+    """Expert counts that are not a multiple of the 128-row weight tile (the tile's last
+    rows belong to the next weight piece and must not be stored), short K, ragged token
+    tiles, the smallest batch of the tensor-core router (T=33) and the largest of the
+    small-batch one (T=32)."""
+    shape = W.MoEShape(d=d, I=128, E=32 * n_group, n_group=n_group, topk_group=min(2, n_group), top_k=8)
+    x = W.make_tokens(shape, T, 4, "cuda")
+    wr, b = W.make_router(shape, 4, "cuda")
+    logits, idx, w = gpu_route(shape, x, wr, b)
+    P.check_logits(shape, x, wr, logits)
+    flagged, _ = P.check_routing(shape, logits, b.cpu().numpy(), idx, w)
+    assert len(flagged) <= max(2, T // 100)
+
+
 @pytest.mark.parametrize("name", ["decode", "prefill", "skewed"])
 def test_beam_route_parity(name):
     shape, T, hot = W.WORKLOADS[name]
