@@ -236,7 +236,7 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
 
     const Shape s = shape_of(cfg);
     const RouterPlan plan = router_plan(s, T, dev->num_sms);
-    const int bn_max = gemm_bn_max(T);
+    const int bn_max = gemm_bn_max(s, T);
     const int max_tiles = dispatch_max_tiles(s, T, bn_max);
     const int rows = T * s.top_k;
     Scratch sc;

@@ -21,8 +21,10 @@
 //
 // Roles (one CTA per SM, persistent over a static round-robin of work items):
 //   warp 0 lane 0: TMA producer - per 64-wide K chunk, the weight tile(s) [128 x 64] and
-//                  the activation rows in boxes of 16 [16 x 64], 128-byte swizzle, into a
-//                  ring of shared-memory stages (full/empty mbarriers);
+//                  the tile's activation rows (rounded up to 16) in the fewest boxes of
+//                  16..256 rows, 128-byte swizzle, into a ring of shared-memory stages
+//                  (full/empty mbarriers). Every TMA copy costs the single issuing thread
+//                  tens of cycles, so fewer, larger boxes keep it ahead of the MMAs;
 //   warp 1:        allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=rows rounded up to
 //                  16, K=16 per instruction) and tcgen05.commit to release stages and to
 //                  publish a finished accumulator;
@@ -46,7 +48,8 @@ namespace {
 constexpr int BM = 128;        // weight rows per tile (MMA M)
 constexpr int BK = 64;         // K per stage: one 128-byte swizzle row of BF16
 constexpr int UK = 16;         // K per tcgen05.mma (kind::f16)
-constexpr int kBoxRows = 16;   // activation rows per TMA box
+constexpr int kBoxRows = 16;   // granule of activation rows (MMA N step, smallest TMA box)
+constexpr int kBoxKinds = 5;   // activation tensor maps with boxes of 16, 32, 64, 128, 256 rows
 #ifndef BEAM_GEMM_EPI_WARPS
 #define BEAM_GEMM_EPI_WARPS 8
 #endif
@@ -99,6 +102,12 @@ struct GemmArgs {
     int* status;            // may be null
 };
 
+// The B operand (token rows) as tensor maps that differ only in box height:
+// m[i] has boxes of (16 << i) rows x 64 columns.
+struct BMaps {
+    CUtensorMap m[kBoxKinds];
+};
+
 struct Item {
     int4 tl;    // {expert, first B row, rows, 0}
     int m;      // weight tile
@@ -142,7 +151,7 @@ __device__ __forceinline__ void record_failure(volatile int* abort_flag, int* st
 template <int kMode, int kBNMax>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                        const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmArgs args) {
+                        const __grid_constant__ BMaps tmB, const __grid_constant__ GemmArgs args) {
     using C = Cfg<kMode, kBNMax>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA0);
         if (kMode == kModeGateUp) ptx::prefetch_tmap(&tmA1);
-        ptx::prefetch_tmap(&tmB);
+        for (int i = 0; i < kBoxKinds && (kBoxRows << i) <= kBNMax; ++i) ptx::prefetch_tmap(&tmB.m[i]);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
@@ -211,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     flag_status(status, kStatusBadIndex);
                     continue;
                 }
-                const int nbox = (it.tl.z + kBoxRows - 1) / kBoxRows;
-                const uint32_t bytes = C::kA * C::kNumA + nbox * kBoxRows * BK * 2;
+                const int b_rows = ((it.tl.z + kBoxRows - 1) / kBoxRows) * kBoxRows;
+                const uint32_t bytes = C::kA * C::kNumA + b_rows * BK * 2;
                 const int a_row = (kMode == kModeRouter ? 0 : it.tl.x * args.rows_per_expert) + it.m * BM;
                 const int kc0 = it.split * k_chunks;
                 for (int kc = 0; kc < k_chunks; ++kc) {
@@ -230,9 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tma_load_2d(sa + j * C::kA, map, kx, row, bar(FULL0 + stage), pol_w);
                     }
                     const uint32_t sb = sa + C::kA * C::kNumA;
-                    for (int j = 0; j < nbox; ++j)
-                        ptx::tma_load_2d(sb + j * kBoxRows * BK * 2, &tmB, kx, it.tl.y + j * kBoxRows,
-                                         bar(FULL0 + stage), pol_x);
+                    // The tile's rows (rounded up to 16) in the fewest boxes: greedy powers
+                    // of two, largest first (at most 4 copies for up to 256 rows).
+                    for (int i = kBoxKinds - 1, r = 0; i >= 0; --i) {
+                        const int h = kBoxRows << i;
+                        if (h > kBNMax || b_rows - r < h) continue;
+                        ptx::tma_load_2d(sb + r * BK * 2, &tmB.m[i], kx, it.tl.y + r, bar(FULL0 + stage), pol_x);
+                        r += h;
+                    }
                     issued |= 1u << stage;
                     parity = (parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) {
@@ -373,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int kMode, int kBNMax>
-cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const GemmArgs& args,
+cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const BMaps& b, const GemmArgs& args,
                         int grid, cudaStream_t st) {
     using C = Cfg<kMode, kBNMax>;
     auto kern = grouped_gemm_kernel<kMode, kBNMax>;
@@ -430,6 +444,21 @@ constexpr int kRouterBN = 128;  // tokens per router N-tile
 
 }  // namespace
 
+namespace {
+// Tensor maps of a [rows, cols] BF16 B operand for every box height up to bn_max.
+bool encode_bmaps(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int bn_max, const char** why) {
+    for (int i = 0; i < kBoxKinds; ++i) {
+        const uint32_t h = kBoxRows << i;
+        if (static_cast<int>(h) > bn_max) {
+            b->m[i] = b->m[0];
+            continue;
+        }
+        if (!encode_tmap_bf16_2d(&b->m[i], base, rows, cols, h, BK, why)) return false;
+    }
+    return true;
+}
+}  // namespace
+
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                          uint32_t box_cols, const char** why) {
     EncodeTiledFn fn = encode_fn();
@@ -451,19 +480,25 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint
     return true;
 }
 
-#ifndef BEAM_GEMM_BN128_MAX_T
-#define BEAM_GEMM_BN128_MAX_T 0
-#endif
-int gemm_bn_max(int T) { return T <= 32 ? 32 : T <= BEAM_GEMM_BN128_MAX_T ? 128 : 256; }
+// N-tile capacity for a batch of T tokens: 32 for decode-sized batches; 128 while the
+// average expert gets at most 32 rows (one tile holds nearly every expert's rows, and the
+// smaller B stage leaves room for a fourth stage); else 256, so that a weight tile is
+// streamed once for up to 256 of its expert's rows.
+int gemm_bn_max(const Shape& s, int T) {
+    if (T <= 32) return 32;
+    const long long avg_rows = static_cast<long long>(T) * s.top_k / s.E;
+    return avg_rows <= 32 ? 128 : 256;
+}
 
 cudaError_t launch_gateup(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* x_perm, int rows,
                           const int4* tiles, int max_tiles, int bn_max, bf16* h, int* status, int num_sms,
                           cudaStream_t st) {
-    CUtensorMap a0, a1, b;
+    CUtensorMap a0, a1;
+    BMaps b;
     const char* why = nullptr;
     if (!encode_tmap_bf16_2d(&a0, w_gate, static_cast<uint64_t>(s.E) * s.I, s.d, BM, BK, &why) ||
         !encode_tmap_bf16_2d(&a1, w_up, static_cast<uint64_t>(s.E) * s.I, s.d, BM, BK, &why) ||
-        !encode_tmap_bf16_2d(&b, x_perm, rows, s.d, kBoxRows, BK, &why))
+        !encode_bmaps(&b, x_perm, rows, s.d, bn_max, &why))
         return cudaErrorInvalidValue;
     const int m_tiles = s.I / BM;
     const GemmArgs args = expert_args(tiles, max_tiles, s.E, rows, m_tiles, s.I, s.d / BK, h, s.I, status);
@@ -475,10 +510,11 @@ cudaError_t launch_gateup(const Shape& s, const bf16* w_gate, const bf16* w_up, 
 
 cudaError_t launch_down(const Shape& s, const bf16* w_down, const bf16* h, int rows, const int4* tiles, int max_tiles,
                         int bn_max, float* y, int* status, int num_sms, cudaStream_t st) {
-    CUtensorMap a0, b;
+    CUtensorMap a0;
+    BMaps b;
     const char* why = nullptr;
     if (!encode_tmap_bf16_2d(&a0, w_down, static_cast<uint64_t>(s.E) * s.d, s.I, BM, BK, &why) ||
-        !encode_tmap_bf16_2d(&b, h, rows, s.I, kBoxRows, BK, &why))
+        !encode_bmaps(&b, h, rows, s.I, bn_max, &why))
         return cudaErrorInvalidValue;
     const int m_tiles = s.d / BM;
     const GemmArgs args = expert_args(tiles, max_tiles, s.E, rows, m_tiles, s.d, s.I / BK, y, s.d, status);
@@ -512,10 +548,11 @@ int router_tc_splits(const Shape& s, int T, int num_sms) {
 
 cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int T, int splits, float* partial,
                              int* status, int num_sms, cudaStream_t st) {
-    CUtensorMap a0, b;
+    CUtensorMap a0;
+    BMaps b;
     const char* why = nullptr;
     if (!encode_tmap_bf16_2d(&a0, w3, 3ull * s.E, s.d, BM, BK, &why) ||
-        !encode_tmap_bf16_2d(&b, x, T, s.d, kBoxRows, BK, &why))
+        !encode_bmaps(&b, x, T, s.d, kRouterBN, &why))
         return cudaErrorInvalidValue;
     const int kc_total = s.d / BK;
     if (splits < 1 || kc_total % splits) return cudaErrorInvalidValue;

@@ -54,7 +54,7 @@ cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src,
 
 // ---------------------------------------------------------------- grouped GEMMs (grouped_gemm.cu)
 // Largest N-tile (tokens per tile) the GEMMs use for a batch of T tokens.
-int gemm_bn_max(int T);
+int gemm_bn_max(const Shape& s, int T);
 // h[rows, I] = silu(x_perm . Wg[e]^T) * (x_perm . Wu[e]^T), per N-tile of the work list.
 cudaError_t launch_gateup(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* x_perm, int rows,
                           const int4* tiles, int max_tiles, int bn_max, bf16* h, int* status, int num_sms,
