@@ -290,3 +290,59 @@ int oracle_forward(const oracle_cfg *cf, const uint16_t *x, int64_t T, const int
     free(l); free(idx); free(w64); free(xd); free(s);
     return rc;
 }
+
+/*
+ * RMSNorm of one row [E] (HF-doc, "Sandwich norms with depth-scaled residuals" bullet:
+ * each block is wrapped in an RMSNorm before and after; the paragraph after the bullets:
+ * RMSNorm scaling is computed in FP32). Written out in FP64:
+ *   y_j = gamma_j * v_j / sqrt( (1/d) sum_i v_i^2 + eps )
+ * Readings (R14): the gain multiplies the normalised vector directly (no "1 + gamma"
+ * offset); eps is an argument (the pages give no value).
+ * gamma is [d] BF16 bits.
+ */
+int oracle_rmsnorm(int d, const double *v, const uint16_t *gamma, double eps, double *y)
+{
+    if (d <= 0 || !v || !gamma || !y || !(eps >= 0.0)) return ORACLE_BAD_ARG;
+    double ss = 0.0;
+    for (int j = 0; j < d; j++) ss += v[j] * v[j];
+    const double r = 1.0 / sqrt(ss / (double)d + eps);
+    for (int j = 0; j < d; j++) y[j] = bf16_value(gamma[j]) * v[j] * r;
+    return ORACLE_OK;
+}
+
+/*
+ * Depth-scaled residual update ([A] Glonce, paragraph on the residual connections: the
+ * input embedding is step 1; at step k the sublayer output is added with weight 1/sqrt(k)
+ * while the existing stream keeps weight sqrt((k-1)/k); HF-doc: after k contributions the
+ * stream is their sum divided by sqrt(k)):
+ *   out_j = sqrt((k-1)/k) * stream_j + sub_j / sqrt(k),   k >= 2.
+ */
+int oracle_residual(int d, int k, const double *stream, const double *sub, double *out)
+{
+    if (d <= 0 || k < 2 || !stream || !sub || !out) return ORACLE_BAD_ARG;
+    const double a = sqrt((double)(k - 1) / (double)k), b = 1.0 / sqrt((double)k);
+    for (int j = 0; j < d; j++) out[j] = a * stream[j] + b * sub[j];
+    return ORACLE_OK;
+}
+
+/* BF16 bit pattern nearest to v (round to nearest, ties to even), for finite v in the
+ * normal range: the significand is cut to 8 bits by rounding in FP64. */
+static uint16_t bf16_round(double v)
+{
+    if (v == 0.0) return (uint16_t)(signbit(v) ? 0x8000u : 0u);
+    int e;
+    double m = frexp(v, &e);                   /* v = m * 2^e, 0.5 <= |m| < 1 */
+    double r = nearbyint(ldexp(m, 8));         /* 8 significant bits, ties to even */
+    float f = (float)ldexp(r, e - 8);          /* exact: 8 bits fit FP32 */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* Rounds n FP64 values to BF16 bit patterns (the MoE block's input is a BF16 hidden state). */
+int oracle_round_bf16(int64_t n, const double *v, uint16_t *out)
+{
+    if (n < 0 || (n && (!v || !out))) return ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < n; i++) out[i] = bf16_round(v[i]);
+    return ORACLE_OK;
+}

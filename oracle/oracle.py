@@ -92,7 +92,11 @@ class Oracle:
         L.oracle_route.argtypes = [cfgp, P, P, i64, P, P, P, P, P, P, P]
         L.oracle_expert.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
         L.oracle_forward.argtypes = [cfgp, P, i64, P, i64, P, P, P, P, P, P, P, P, P, P]
-        for f in (L.oracle_check_cfg, L.oracle_router_logits, L.oracle_route, L.oracle_expert, L.oracle_forward):
+        L.oracle_rmsnorm.argtypes = [ctypes.c_int, P, P, ctypes.c_double, P]
+        L.oracle_residual.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P]
+        L.oracle_round_bf16.argtypes = [i64, P, P]
+        for f in (L.oracle_check_cfg, L.oracle_router_logits, L.oracle_route, L.oracle_expert, L.oracle_forward,
+                  L.oracle_rmsnorm, L.oracle_residual, L.oracle_round_bf16):
             f.restype = ctypes.c_int
         self.L = L
         self.path = path
@@ -177,6 +181,55 @@ class Oracle:
         return out, idx, w
 
 
+    def rmsnorm(self, v, gamma_bits, eps) -> np.ndarray:
+        """RMSNorm of one FP64 row with a BF16 gain (bit patterns): FP64 result."""
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        g = _u16(gamma_bits)
+        assert g.shape == v.shape
+        y = np.empty_like(v)
+        _check(self.L.oracle_rmsnorm(v.shape[0], _ptr(v), _ptr(g), float(eps), _ptr(y)), "rmsnorm")
+        return y
+
+    def residual(self, stream, sub, k) -> np.ndarray:
+        """Depth-scaled residual update for contribution k (>= 2): FP64 row."""
+        stream = np.ascontiguousarray(stream, dtype=np.float64)
+        sub = np.ascontiguousarray(sub, dtype=np.float64)
+        out = np.empty_like(stream)
+        _check(self.L.oracle_residual(stream.shape[0], int(k), _ptr(stream), _ptr(sub), _ptr(out)), "residual")
+        return out
+
+    def round_bf16(self, v) -> np.ndarray:
+        """BF16 bit patterns nearest to FP64 values (same shape)."""
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        out = np.empty(v.shape, np.uint16)
+        _check(self.L.oracle_round_bf16(v.size, _ptr(v), _ptr(out)), "round_bf16")
+        return out
+
+    def sublayer(self, shape, stream_bits, pre_gamma_bits, post_gamma_bits, eps, k, bias, experts, tokens,
+                 x_bits=None, logits=None, router_w=None, idx_in=None):
+        """The MoE sublayer for the rows `tokens` of a BF16 stream [T, d] (bit patterns),
+        in the pages' order: x = RMSNorm_pre(stream) rounded to BF16 (the block's input
+        hidden state), m = MoE(x), out = sqrt((k-1)/k) stream + RMSNorm_post(m) / sqrt(k).
+        x_bits [T, d], if given, replaces the oracle's own rounded pre-norm output (so the
+        rest can be checked given another implementation's BF16 input); logits / idx_in as
+        in forward(). Returns (out [n, d] FP64, x_rows [n, d] FP64 pre-norm before rounding)."""
+        stream_bits = _u16(stream_bits)
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        T, d = stream_bits.shape
+        s64 = stream_bits[tokens].astype(np.uint32) << 16
+        s64 = s64.view(np.float32).astype(np.float64)
+        x_rows = np.stack([self.rmsnorm(s64[i], pre_gamma_bits, eps) for i in range(len(tokens))]) \
+            if len(tokens) else np.zeros((0, d))
+        if x_bits is None:
+            x_bits = np.zeros((T, d), np.uint16)
+            x_bits[tokens] = self.round_bf16(x_rows)
+        m, _, _ = self.forward(shape, x_bits, bias, experts, tokens=tokens, router_w=router_w, logits=logits,
+                               idx_in=idx_in)
+        out = np.stack([self.residual(s64[i], self.rmsnorm(m[i], post_gamma_bits, eps), k)
+                        for i in range(len(tokens))]) if len(tokens) else np.zeros((0, d))
+        return out, x_rows
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -199,6 +252,22 @@ def expert(*a, **k):
 
 def forward(*a, **k):
     return default().forward(*a, **k)
+
+
+def rmsnorm(*a, **k):
+    return default().rmsnorm(*a, **k)
+
+
+def residual(*a, **k):
+    return default().residual(*a, **k)
+
+
+def round_bf16(*a, **k):
+    return default().round_bf16(*a, **k)
+
+
+def sublayer(*a, **k):
+    return default().sublayer(*a, **k)
 
 
 def bf16_bits(t) -> np.ndarray:

@@ -240,9 +240,94 @@ def check_given_selection(orc, seed=12):
         np.testing.assert_allclose(w[t], ws, rtol=2e-6)
 
 
+# ---------------------------------------------------------------- sandwich norm and residual
+
+def pin_rmsnorm_library(O):
+    """RMSNorm equals torch.nn.functional.rms_norm in float64 (an independent library
+    routine), for several widths, scales and eps."""
+    rng = np.random.default_rng(11)
+    for d, scale, eps in ((8, 1.0, 1e-6), (512, 3.0, 1e-5), (5120, 0.02, 1e-6), (96, 1e-3, 1e-2)):
+        v = rng.standard_normal(d) * scale
+        gamma = torch.randn(d, dtype=torch.float32).to(torch.bfloat16)
+        got = O.rmsnorm(v, _bits(gamma), eps)
+        want = torch.nn.functional.rms_norm(torch.from_numpy(v), (d,), weight=gamma.double(), eps=eps).numpy()
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-15)
+
+
+def pin_rmsnorm_closed_forms(O):
+    """Constant row c: gamma * c / sqrt(c^2 + eps). Scale invariance: rmsnorm(s v) =
+    rmsnorm(v) when eps = 0. Unit gain on a row of RMS 1 with eps = 0: the row itself."""
+    d = 64
+    gamma = torch.full((d,), 1.5, dtype=torch.bfloat16)
+    for c in (-2.0, 0.25, 7.0):
+        got = O.rmsnorm(np.full(d, c), _bits(gamma), 1e-3)
+        np.testing.assert_allclose(got, 1.5 * c / np.sqrt(c * c + 1e-3), rtol=1e-14)
+    rng = np.random.default_rng(12)
+    v = rng.standard_normal(d)
+    g1 = torch.ones(d, dtype=torch.bfloat16)
+    np.testing.assert_allclose(O.rmsnorm(37.0 * v, _bits(g1), 0.0), O.rmsnorm(v, _bits(g1), 0.0), rtol=1e-13)
+    u = v / np.sqrt(np.mean(v * v))
+    np.testing.assert_allclose(O.rmsnorm(u, _bits(g1), 0.0), u, rtol=1e-13)
+
+
+def pin_residual_is_scaled_sum(O):
+    """Depth-scaled residual: starting from the embedding (contribution 1) and adding
+    contributions 2..K one step at a time gives the sum of all K divided by sqrt(K), the
+    statement of the transformers doc; the stream keeps unit RMS when the contributions
+    are orthonormal."""
+    rng = np.random.default_rng(13)
+    d, K = 32, 9
+    parts = rng.standard_normal((K, d))
+    stream = parts[0].copy()
+    for k in range(2, K + 1):
+        stream = O.residual(stream, parts[k - 1], k)
+    np.testing.assert_allclose(stream, parts.sum(axis=0) / np.sqrt(K), rtol=1e-12, atol=1e-13)
+    q, _ = np.linalg.qr(rng.standard_normal((d, K)))
+    stream = q[:, 0] * np.sqrt(d)
+    for k in range(2, K + 1):
+        stream = O.residual(stream, q[:, k - 1] * np.sqrt(d), k)
+        np.testing.assert_allclose(np.sqrt(np.mean(stream * stream)), 1.0, rtol=1e-12)
+
+
+def pin_round_bf16_vs_torch(O):
+    """The oracle's BF16 rounding equals torch's FP32 -> BF16 conversion (round to nearest,
+    ties to even) on values that are exact in FP32, including exact ties."""
+    rng = np.random.default_rng(14)
+    v32 = (rng.standard_normal(4000) * np.exp(rng.uniform(-20, 20, 4000))).astype(np.float32)
+    ties = (np.float32(1.0) + np.arange(1, 200, dtype=np.float32) * np.float32(2.0 ** -8)).astype(np.float32)
+    v32 = np.concatenate([v32, ties, -ties, np.float32([0.0, 1.0, -2.5, 65504.0])])
+    want = torch.from_numpy(v32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(O.round_bf16(v32.astype(np.float64)), want)
+
+
+def pin_sublayer_composition(O, seed=15):
+    """Whole sublayer with identical experts (routing drops out: the MoE output is
+    2.5 * expert(x)), against torch float64 in the pages' order: pre-RMSNorm, BF16 input,
+    SwiGLU expert, x2.5, post-RMSNorm, depth-scaled residual with k = 7."""
+    shape = W.TINY
+    T, k, eps = 6, 7, 1e-6
+    g = torch.Generator().manual_seed(seed)
+    stream = torch.randn((T, shape.d), generator=g).mul_(3.0).to(torch.bfloat16)
+    pre = (1.0 + 0.1 * torch.randn(shape.d, generator=g)).to(torch.bfloat16)
+    post = (1.0 + 0.1 * torch.randn(shape.d, generator=g)).to(torch.bfloat16)
+    wr, b = W.make_router(shape, seed)
+    wg1, wu1, wd1 = (w[3] for w in W.make_experts(shape, seed))
+    experts = lambda e: (_bits(wg1), _bits(wu1), _bits(wd1))  # noqa: E731
+    out, _ = O.sublayer(shape, _bits(stream), _bits(pre), _bits(post), eps, k, b.numpy(), experts,
+                        np.arange(T), router_w=wr.numpy())
+    s64 = stream.double()
+    x = torch.nn.functional.rms_norm(s64, (shape.d,), weight=pre.double(), eps=eps).float().to(torch.bfloat16)
+    m = 2.5 * _torch_expert(x.double(), wg1, wu1, wd1)
+    y = torch.nn.functional.rms_norm(m, (shape.d,), weight=post.double(), eps=eps)
+    want = math.sqrt((k - 1) / k) * s64 + y / math.sqrt(k)
+    np.testing.assert_allclose(out, want.numpy(), rtol=1e-9, atol=1e-9)
+
+
 ALL_CHECKS = [
     check_golden_cases, check_invariants, check_sigmoid_and_bias, check_group_scores_vs_topk,
     check_group_choice_brute_force, check_selection_brute_force_small, check_plain_topk_reduction,
     check_logits_vs_matmul, check_expert_vs_torch, check_forward_combination, check_zero_input,
     check_identical_experts, check_given_selection,
+    pin_rmsnorm_library, pin_rmsnorm_closed_forms, pin_residual_is_scaled_sum, pin_round_bf16_vs_torch,
+    pin_sublayer_composition,
 ]

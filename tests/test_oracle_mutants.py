@@ -27,6 +27,14 @@ MUTANTS = [
     ("logits_transposed", "(double)wr[(int64_t)e * c->d + j]", "(double)wr[(int64_t)j * c->E + e]"),
     ("logits_kept_fp64_sigmoid_in_fp32", "s[e] = (float)(1.0 / (1.0 + exp(-(double)l[e])));",
      "s[e] = 1.0f / (1.0f + (float)exp(-(double)l[e]) * 1.0000005f);"),
+    ("residual_weights_swapped", "const double a = sqrt((double)(k - 1) / (double)k), b = 1.0 / sqrt((double)k);",
+     "const double b = sqrt((double)(k - 1) / (double)k), a = 1.0 / sqrt((double)k);"),
+    ("residual_step_off_by_one", "const double a = sqrt((double)(k - 1) / (double)k), b = 1.0 / sqrt((double)k);",
+     "const double a = sqrt((double)(k - 2) / (double)(k - 1)), b = 1.0 / sqrt((double)(k - 1));"),
+    ("rmsnorm_sum_not_mean", "1.0 / sqrt(ss / (double)d + eps)", "1.0 / sqrt(ss + eps)"),
+    ("rmsnorm_eps_dropped", "1.0 / sqrt(ss / (double)d + eps)", "1.0 / sqrt(ss / (double)d)"),
+    ("rmsnorm_gain_dropped", "y[j] = bf16_value(gamma[j]) * v[j] * r;", "y[j] = v[j] * r;"),
+    ("bf16_truncates", "double r = nearbyint(ldexp(m, 8));", "double r = trunc(ldexp(m, 8));"),
 ]
 
 
