@@ -110,6 +110,36 @@ BEAM_MOE_API int beam_moe_forward_ex(const beam_moe_config *cfg, const __nv_bflo
                         const float *expert_bias, const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up,
                         const __nv_bfloat16 *w_down, int T, __nv_bfloat16 *out, cudaStream_t stream);
 
+/* Pre-norm of the MoE sublayer (transformers "Beam" doc, Overview, "Sandwich norms with
+ * depth-scaled residuals" bullet: each block is wrapped in an RMSNorm before and after;
+ * the paragraph after the bullets: RMSNorm scaling is computed in FP32):
+ *   out[t][j] = gamma[j] * v[t][j] / sqrt( (1/d) sum_i v[t][i]^2 + eps ),  FP32, rounded to BF16.
+ * Readings: the gain multiplies the normalised row directly; eps is the caller's (the
+ * pages give no value).
+ *   v, out  bf16 [T, d], rows contiguous; gamma bf16 [d]; d a multiple of 4, at most 8192.
+ * out may equal v (in place). Deterministic (fixed reduction order). */
+BEAM_MOE_API int beam_moe_rmsnorm(int d, const __nv_bfloat16 *v, const __nv_bfloat16 *gamma, float eps, int T,
+                     __nv_bfloat16 *out, cudaStream_t stream);
+
+/* The whole MoE sublayer of a decoder layer on the residual stream: sandwich norms around
+ * the MoE block and the depth-scaled residual (same bullet; Glonce "Reflection releases
+ * Beam ...", paragraph on the residual connections: counting the input embedding as step
+ * 1, step k adds the sublayer output with weight 1/sqrt(k) and keeps the stream with
+ * weight sqrt((k-1)/k)):
+ *   x   = RMSNorm(stream_in; pre_gamma, eps)                       (BF16, as beam_moe_rmsnorm)
+ *   m   = MoE block of beam_moe_forward_ex on x, kept in FP32 (not rounded to BF16)
+ *   stream_out = sqrt((k-1)/k) stream_in + RMSNorm(m; post_gamma, eps) / sqrt(k)   (FP32 -> BF16)
+ * The post-norm and the residual update run fused into the combine kernel.
+ *   stream_in, stream_out  bf16 [T, d]; pre_gamma, post_gamma bf16 [d]; k >= 2 is this
+ *   sublayer's contribution index (the MoE sublayer of decoder layer l, 0-based, is
+ *   k = 2l + 3 when every layer has an attention and an MLP sublayer); d <= 8192.
+ * stream_out may equal stream_in (in-place update); other outputs must not alias inputs. */
+BEAM_MOE_API int beam_moe_sublayer_forward(const beam_moe_config *cfg, const __nv_bfloat16 *stream_in,
+                              const __nv_bfloat16 *pre_gamma, const __nv_bfloat16 *post_gamma, float eps, int k,
+                              const float *router_w, const float *expert_bias, const __nv_bfloat16 *w_gate,
+                              const __nv_bfloat16 *w_up, const __nv_bfloat16 *w_down, int T,
+                              __nv_bfloat16 *stream_out, cudaStream_t stream);
+
 /* Router with no device allocation. The release pages have no counterpart: this is a
  * deployment variant of beam_moe_route_ex for callers that must not have a library
  * allocate device memory (an engine that has claimed all free HBM for weights and KV
@@ -147,9 +177,10 @@ BEAM_MOE_API int beam_moe_device_status(cudaStream_t stream);
 /* Per-stage timing for profiling. While enabled (per thread), each forward/route call
  * records CUDA events on its stream around each stage; beam_moe_timing_read synchronises
  * on the last call's final event and writes up to max_stages durations in milliseconds
- * (stage order: router weight split, router logits, router select, dispatch count,
- * dispatch scan, dispatch scatter, gather, gate/up GEMM, down GEMM, combine; unrun stages
- * read 0). Returns the number of stages, or a negative error. */
+ * (stage order: pre-norm, router weight split, router logits, router select, dispatch count,
+ * dispatch scan, dispatch scatter, gather, gate/up GEMM, down GEMM, combine (fused with the
+ * post-norm and residual in beam_moe_sublayer_forward); unrun stages read 0). Returns the
+ * number of stages, or a negative error. */
 BEAM_MOE_API int beam_moe_timing_enable(int enable);
 BEAM_MOE_API int beam_moe_timing_read(float *ms, int max_stages);
 

@@ -24,14 +24,14 @@ BEAM_MOE_MAX_TOKENS = 262144
 BEAM_MOE_NOALLOC_MAX_TOKENS = 8192
 BEAM_MOE_NOALLOC_SCRATCH_BYTES = 40 << 20
 
-STAGES = ("router_split", "router_logits", "router_select", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather",
+STAGES = ("pre_norm", "router_split", "router_logits", "router_select", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather",
           "gateup_gemm", "down_gemm", "combine")
 
 # Every symbol include/beam_moe.h declares.
 EXPORTS = ("beam_moe_default_config", "beam_moe_route", "beam_moe_route_ex", "beam_moe_forward",
            "beam_moe_forward_ex", "beam_moe_router_logits", "beam_moe_last_error", "beam_moe_device_status",
            "beam_moe_timing_enable", "beam_moe_timing_read", "beam_moe_last_launch_count",
-           "beam_moe_route_noalloc")
+           "beam_moe_route_noalloc", "beam_moe_rmsnorm", "beam_moe_sublayer_forward")
 
 
 class BeamMoeConfig(ctypes.Structure):
@@ -72,6 +72,9 @@ def load() -> ctypes.CDLL:
             L.beam_moe_forward_ex.argtypes = [cfgp, P, P, P, P, P, P, i, P, P]
             L.beam_moe_router_logits.argtypes = [cfgp, P, P, i, P, P]
             L.beam_moe_route_noalloc.argtypes = [cfgp, P, P, P, i, P, P, P]
+            f32 = ctypes.c_float
+            L.beam_moe_rmsnorm.argtypes = [i, P, P, f32, i, P, P]
+            L.beam_moe_sublayer_forward.argtypes = [cfgp, P, P, P, f32, i, P, P, P, P, P, i, P, P]
             L.beam_moe_last_error.restype = ctypes.c_char_p
             L.beam_moe_last_error.argtypes = []
             L.beam_moe_device_status.argtypes = [P]
@@ -80,7 +83,8 @@ def load() -> ctypes.CDLL:
             L.beam_moe_last_launch_count.argtypes = []
             for f in ("beam_moe_route", "beam_moe_route_ex", "beam_moe_forward", "beam_moe_forward_ex",
                       "beam_moe_router_logits", "beam_moe_device_status", "beam_moe_timing_enable",
-                      "beam_moe_timing_read", "beam_moe_last_launch_count", "beam_moe_route_noalloc"):
+                      "beam_moe_timing_read", "beam_moe_last_launch_count", "beam_moe_route_noalloc",
+                      "beam_moe_rmsnorm", "beam_moe_sublayer_forward"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -144,6 +148,19 @@ def beam_moe_route_noalloc(cfg, x, router_w, expert_bias, T, topk_idx, topk_w, s
     library; T <= BEAM_MOE_NOALLOC_MAX_TOKENS)."""
     return _check(load().beam_moe_route_noalloc(_cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), int(T),
                                                 _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
+def beam_moe_rmsnorm(d, v, gamma, eps, T, out, stream=None):
+    return _check(load().beam_moe_rmsnorm(int(d), _ptr(v), _ptr(gamma), float(eps), int(T), _ptr(out),
+                                          _stream(stream)))
+
+
+def beam_moe_sublayer_forward(cfg, stream_in, pre_gamma, post_gamma, eps, k, router_w, expert_bias, w_gate, w_up,
+                              w_down, T, stream_out, stream=None):
+    return _check(load().beam_moe_sublayer_forward(_cfg(cfg), _ptr(stream_in), _ptr(pre_gamma), _ptr(post_gamma),
+                                                   float(eps), int(k), _ptr(router_w), _ptr(expert_bias),
+                                                   _ptr(w_gate), _ptr(w_up), _ptr(w_down), int(T), _ptr(stream_out),
+                                                   _stream(stream)))
 
 
 def beam_moe_router_logits(cfg, x, router_w, T, logits, stream=None):

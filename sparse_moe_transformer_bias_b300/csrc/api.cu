@@ -76,7 +76,7 @@ int check_stream(cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------- stage timing
-enum Stage { kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kGateUp, kDown, kCombine, kNumStages };
+enum Stage { kPreNorm, kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kGateUp, kDown, kCombine, kNumStages };
 struct Timing {
     bool enabled = false;
     bool created = false;
@@ -132,6 +132,7 @@ int check_ptr(const void* p, const char* name) {
 Shape shape_of(const beam_moe_config* c) { return Shape{c->d, c->I, c->E, c->n_group, c->topk_group, c->top_k, c->scale}; }
 
 struct Scratch {
+    bf16* x_norm = nullptr;
     bf16* w3 = nullptr;
     float* partial = nullptr;
     int32_t* idx = nullptr;
@@ -159,10 +160,11 @@ struct Carver {
 };
 
 // Lays scratch out from `base` (nullptr: size only). Returns the byte count.
-size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool forward, bool route_out, char* base,
-              Scratch* sc) {
+size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool forward, bool route_out,
+              bool pre_norm, char* base, Scratch* sc) {
     Carver c{base};
     const size_t pairs = static_cast<size_t>(T) * s.top_k;
+    sc->x_norm = pre_norm ? c.take<bf16>(static_cast<size_t>(T) * s.d) : nullptr;
     sc->w3 = plan.w3_elems ? c.take<bf16>(plan.w3_elems) : nullptr;
     sc->partial = c.take<float>(static_cast<size_t>(plan.splits) * T * s.E);
     if (route_out) {
@@ -194,20 +196,37 @@ size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool
         }                                                                                           \
     } while (0)
 
-// mode 0: route (outputs topk_idx/topk_w); 1: logits only; 2: forward.
+// The MoE sublayer's extra inputs (mode 3).
+struct SublayerArgs {
+    const bf16* pre_gamma;
+    const bf16* post_gamma;
+    float eps;
+    int k;
+};
+
+// mode 0: route (outputs topk_idx/topk_w); 1: logits only; 2: forward; 3: sublayer (x is
+// the residual stream: pre-norm, forward, then combine fused with the post-norm and the
+// residual update into out).
 int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float* bias, const bf16* wg,
         const bf16* wu, const bf16* wd, int T, int32_t* topk_idx, float* topk_w, float* logits, bf16* out, int mode,
-        cudaStream_t st) {
+        cudaStream_t st, const SublayerArgs* sub = nullptr) {
     g_launches = 0;
     timing_begin_call();
     int rc;
-    if ((rc = check_cfg(cfg)) || (rc = check_T(T)) || (rc = check_ptr(x, "x")) || (rc = check_ptr(wr, "router_w")))
+    if ((rc = check_cfg(cfg)) || (rc = check_T(T)) || (rc = check_ptr(x, mode == 3 ? "stream_in" : "x")) ||
+        (rc = check_ptr(wr, "router_w")))
         return rc;
+    if (mode == 3) {
+        if ((rc = check_ptr(sub->pre_gamma, "pre_gamma")) || (rc = check_ptr(sub->post_gamma, "post_gamma"))) return rc;
+        if (!(sub->eps >= 0.f) || !std::isfinite(sub->eps)) return fail(BEAM_MOE_ERR_ARG, "eps must be finite and >= 0");
+        if (sub->k < 2) return fail(BEAM_MOE_ERR_ARG, "k=%d must be >= 2 (the embedding is contribution 1)", sub->k);
+        if (cfg->d > kNormMaxD) return fail(BEAM_MOE_ERR_ARG, "d=%d exceeds the sublayer limit %d", cfg->d, kNormMaxD);
+    }
     if (mode != 1 && (rc = check_ptr(bias, "expert_bias"))) return rc;
     if (mode == 0 && ((rc = check_ptr(topk_idx, "topk_idx")) || (rc = check_ptr(topk_w, "topk_w")))) return rc;
     if (mode == 1 && (rc = check_ptr(logits, "logits"))) return rc;
-    if (mode == 2 && ((rc = check_ptr(wg, "w_gate")) || (rc = check_ptr(wu, "w_up")) ||
-                      (rc = check_ptr(wd, "w_down")) || (rc = check_ptr(out, "out"))))
+    if (mode >= 2 && ((rc = check_ptr(wg, "w_gate")) || (rc = check_ptr(wu, "w_up")) ||
+                      (rc = check_ptr(wd, "w_down")) || (rc = check_ptr(out, mode == 3 ? "stream_out" : "out"))))
         return rc;
     if (T == 0) return BEAM_MOE_OK;
     if ((rc = check_stream(st))) return rc;
@@ -240,19 +259,25 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     const int max_tiles = dispatch_max_tiles(s, T, bn_max);
     const int rows = T * s.top_k;
     Scratch sc;
-    const size_t bytes = layout(s, T, plan, max_tiles, mode == 2, mode != 0, nullptr, &sc);
+    const bool fwd = mode >= 2;
+    const size_t bytes = layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, nullptr, &sc);
     void* mem = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, st);
     if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "scratch allocation of %zu bytes: %s", bytes, cudaGetErrorString(e));
-    layout(s, T, plan, max_tiles, mode == 2, mode != 0, static_cast<char*>(mem), &sc);
+    layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, static_cast<char*>(mem), &sc);
     {
         int32_t* idx = mode == 0 ? topk_idx : sc.idx;
         float* w = mode == 0 ? topk_w : sc.w;
+        const bf16* stream_in = x;
+        if (mode == 3) {
+            LAUNCH(kPreNorm, launch_rmsnorm(s.d, stream_in, sub->pre_gamma, sub->eps, T, sc.x_norm, st));
+            x = sc.x_norm;
+        }
         if (plan.tensor) LAUNCH(kSplitW, launch_router_split_weights(s, wr, sc.w3, dev->num_sms, st));
         LAUNCH(kLogits, launch_router_logits(s, plan, x, wr, T, sc.w3, sc.partial, dev->status, dev->num_sms, st));
         LAUNCH(kSelect, launch_router_select(s, sc.partial, plan.splits, mode == 1 ? nullptr : bias, T, idx, w,
                                              mode == 1 ? logits : nullptr, st));
-        if (mode == 2) {
+        if (fwd) {
             LAUNCH(kCount, launch_dispatch_count(s, idx, T, sc.chunk, dev->status, st));
             LAUNCH(kScan, launch_dispatch_scan(s, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, st));
             LAUNCH(kScatter, launch_dispatch_scatter(s, idx, T, sc.chunk, sc.perm_src, sc.inv_slot, dev->status, st));
@@ -261,7 +286,11 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
                                           dev->num_sms, st));
             LAUNCH(kDown, launch_down(s, wd, sc.h, rows, sc.tiles, max_tiles, bn_max, sc.y, dev->status,
                                       dev->num_sms, st));
-            LAUNCH(kCombine, launch_combine(s, sc.y, sc.inv_slot, w, T, out, dev->status, st));
+            if (mode == 3)
+                LAUNCH(kCombine, launch_combine_residual(s, sc.y, sc.inv_slot, w, T, stream_in, sub->post_gamma,
+                                                         sub->eps, sub->k, out, dev->status, st));
+            else
+                LAUNCH(kCombine, launch_combine(s, sc.y, sc.inv_slot, w, T, out, dev->status, st));
         }
     }
     rc = BEAM_MOE_OK;
@@ -326,6 +355,34 @@ int beam_moe_forward(const __nv_bfloat16* x, const float* router_w, const float*
                      __nv_bfloat16* out, cudaStream_t stream) {
     const beam_moe_config c = beam_moe_default_config();
     return beam_moe_forward_ex(&c, x, router_w, expert_bias, w_gate, w_up, w_down, T, out, stream);
+}
+
+int beam_moe_sublayer_forward(const beam_moe_config* cfg, const __nv_bfloat16* stream_in,
+                              const __nv_bfloat16* pre_gamma, const __nv_bfloat16* post_gamma, float eps, int k,
+                              const float* router_w, const float* expert_bias, const __nv_bfloat16* w_gate,
+                              const __nv_bfloat16* w_up, const __nv_bfloat16* w_down, int T, __nv_bfloat16* stream_out,
+                              cudaStream_t stream) {
+    const SublayerArgs sub{pre_gamma, post_gamma, eps, k};
+    return run(cfg, stream_in, router_w, expert_bias, w_gate, w_up, w_down, T, nullptr, nullptr, nullptr, stream_out, 3,
+               stream, &sub);
+}
+
+int beam_moe_rmsnorm(int d, const __nv_bfloat16* v, const __nv_bfloat16* gamma, float eps, int T,
+                     __nv_bfloat16* out, cudaStream_t stream) {
+    g_launches = 0;
+    timing_begin_call();
+    int rc;
+    if (d < 4 || d % 4 || d > kNormMaxD) return fail(BEAM_MOE_ERR_ARG, "d=%d must be a multiple of 4 in [4, %d]", d, kNormMaxD);
+    if ((rc = check_T(T)) || (rc = check_ptr(v, "v")) || (rc = check_ptr(gamma, "gamma")) ||
+        (rc = check_ptr(out, "out")))
+        return rc;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(BEAM_MOE_ERR_ARG, "eps must be finite and >= 0");
+    if (T == 0) return BEAM_MOE_OK;
+    if ((rc = check_stream(stream))) return rc;
+    const cudaError_t e = launch_rmsnorm(d, v, gamma, eps, T, out, stream);
+    ++g_launches;
+    if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "launch of rmsnorm failed: %s", cudaGetErrorString(e));
+    return BEAM_MOE_OK;
 }
 
 int beam_moe_router_logits(const beam_moe_config* cfg, const __nv_bfloat16* x, const float* router_w, int T,

@@ -80,6 +80,18 @@ int abi_check_config(const beam_moe_config* cfg);
 int abi_check_ptr(const void* p, const char* name);
 int abi_check_stream(cudaStream_t st);
 
+// ---------------------------------------------------------------- sandwich norm (norm.cu)
+// Largest row width the norm kernels take.
+constexpr int kNormMaxD = 8192;
+// out[t] = gamma * v[t] / sqrt(mean(v[t]^2) + eps), FP32, BF16 rows of width d (d % 4 == 0).
+cudaError_t launch_rmsnorm(int d, const bf16* v, const bf16* gamma, float eps, int T, bf16* out, cudaStream_t st);
+// Combine fused with the post-norm and the depth-scaled residual of contribution k:
+// stream_out[t] = sqrt((k-1)/k) stream_in[t] + gamma * m / sqrt(mean(m^2) + eps) / sqrt(k),
+// m = sum_k w[t,k] y[slot(t,k)] in FP32.
+cudaError_t launch_combine_residual(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T,
+                                    const bf16* stream_in, const bf16* gamma, float eps, int k_contrib,
+                                    bf16* stream_out, int* status, cudaStream_t st);
+
 // Host helper: encode a 2-D BF16 tensor map (rows x cols, row-major) with the 128-byte
 // swizzle and a box of box_cols x box_rows. Returns false if the driver refuses it.
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,

@@ -4,6 +4,8 @@
     idx, w = moe.route(x, router_w, bias, shape=workloads.TINY)
     logits = moe.router_logits(x, router_w)
     out = moe.forward_host(x_pinned, ...)     # host in, host out (copies on the stream)
+    x = moe.rmsnorm(stream, gamma, eps)
+    new_stream = moe.sublayer_forward(stream, pre_gamma, post_gamma, eps, k, router_w, bias, w_gate, w_up, w_down)
 
 All compute runs in libbeam_moe.so; nothing here touches the numbers.
 """
@@ -68,3 +70,30 @@ def forward_host(x_host, router_w, bias, w_gate, w_up, w_down, shape: MoEShape =
         out_host.copy_(out_dev, non_blocking=True)
     stream.synchronize()
     return out_host
+
+
+def rmsnorm(v, gamma, eps: float, out=None, stream=None):
+    """RMSNorm of the rows of a BF16 [T, d] tensor with a BF16 gain [d]."""
+    T, d = v.shape
+    assert v.dtype == torch.bfloat16 and v.is_cuda and v.is_contiguous()
+    assert gamma.dtype == torch.bfloat16 and gamma.shape == (d,) and gamma.is_contiguous()
+    if out is None:
+        out = torch.empty_like(v)
+    abi.beam_moe_rmsnorm(d, v, gamma, eps, T, out, stream)
+    return out
+
+
+def sublayer_forward(stream_in, pre_gamma, post_gamma, eps: float, k: int, router_w, bias, w_gate, w_up, w_down,
+                     shape: MoEShape = BEAM, out=None, stream=None):
+    """The MoE sublayer on the residual stream: pre-norm, MoE block, post-norm and the
+    depth-scaled residual for contribution k. out may be stream_in (in place)."""
+    T = _check_inputs(shape, stream_in, router_w, bias)
+    for g in (pre_gamma, post_gamma):
+        assert g.dtype == torch.bfloat16 and g.shape == (shape.d,) and g.is_contiguous()
+    for w, rows, cols in ((w_gate, shape.I, shape.d), (w_up, shape.I, shape.d), (w_down, shape.d, shape.I)):
+        assert w.dtype == torch.bfloat16 and w.shape == (shape.E, rows, cols) and w.is_contiguous()
+    if out is None:
+        out = torch.empty_like(stream_in)
+    abi.beam_moe_sublayer_forward(shape, stream_in, pre_gamma, post_gamma, eps, k, router_w, bias, w_gate, w_up,
+                                  w_down, T, out, stream)
+    return out

@@ -121,8 +121,9 @@ def test_launch_count_and_stage_timing():
         times = abi.beam_moe_timing_read()
     finally:
         abi.beam_moe_timing_enable(False)
-    assert n == len(abi.STAGES)
-    assert all(v > 0 for v in times.values()), times
+    ran = {k for k, v in times.items() if v > 0}
+    assert n == len(ran), (n, times)
+    assert set(abi.STAGES) - ran <= {"pre_norm"}, times   # the plain forward has no pre-norm
 
 
 def test_host_buffers_end_to_end():
