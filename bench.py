@@ -41,9 +41,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch of the dominant kernel from ncu captures (see
 # profiles/); remove an entry when its kernel changes after the capture. Keys: workload name.
-# decode: the E=32 capture read 52.6 MB per touched expert; scaled to the 89 experts the
-# decode batch touches.
-TRAFFIC = {"decode": {"kernel": "gateup_gemm", "bytes": 4.6813e9}}
+# decode: the E=32 capture (profiles/grouped_gemm_decode_E32_T16.md) read 52.47 MB per
+# touched expert and wrote 3.4 MB; scaled to the 89 experts the decode batch touches.
+TRAFFIC = {"decode": {"kernel": "gateup_gemm", "bytes": 52.47e6 * 89 + 3.4e6 * 89 / 32}}
 
 
 def peaks():
