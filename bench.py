@@ -39,9 +39,9 @@ METRIC = "Beam MoE-layer tokens/s (T=16 decode, T=4096 prefill); % of roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes (read + write) per launch of the dominant kernel from ncu captures (see
-# profiles/); remove an entry when its kernel changes after the capture. Keys: workload name.
-# decode: the E=32 capture (profiles/grouped_gemm_decode_E32_T16.md) read 52.47 MB per
+# DRAM bytes (read + write) per launch of the dominant kernel from ncu captures; remove an
+# entry when its kernel changes after the capture. Keys: workload name.
+# decode: an `ncu --set full` capture of the decode GEMMs on 32 experts read 52.47 MB per
 # touched expert and wrote 3.4 MB; scaled to the 89 experts the decode batch touches.
 TRAFFIC = {"decode": {"kernel": "gateup_gemm", "bytes": 52.47e6 * 89 + 3.4e6 * 89 / 32}}
 
