@@ -41,9 +41,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch of the dominant kernel from ncu captures; remove an
 # entry when its kernel changes after the capture. Keys: workload name.
-# decode: an `ncu --set full` capture of the decode GEMMs on 32 experts read 52.47 MB per
-# touched expert and wrote 3.4 MB; scaled to the 89 experts the decode batch touches.
-TRAFFIC = {"decode": {"kernel": "gateup_gemm", "bytes": 52.47e6 * 89 + 3.4e6 * 89 / 32}}
+# decode: an `ncu --set full` capture of the expert kernel on 32 experts read 2.517993 GB
+# and wrote 4.866 MB (per touched expert: 78.69 MB + 0.152 MB); a full launch moves that
+# per touched expert.
+TRAFFIC = {"decode": {"kernel": "expert_mlp", "bytes_per_touched_expert": (2.517993e9 + 4.866304e6) / 32}}
 
 
 def peaks():
@@ -133,13 +134,15 @@ def make_layer(shape, T, hot, device, experts=None, seed=0):
 
 
 def algorithmic(shape, T, n_touched, rows):
-    """Algorithmic FLOPs and bytes of the whole layer and of each GEMM (one launch each)."""
+    """Algorithmic FLOPs and bytes of the whole layer and of the expert kernel (one launch:
+    gate/up + SwiGLU and down over the touched experts' weights)."""
     d, I, E, K = shape.d, shape.I, shape.E, shape.top_k
     layer_flops = T * (K * 3 * 2 * d * I + 2 * d * E)
     layer_bytes = n_touched * 3 * d * I * 2 + E * d * 4 + E * 4 + 2 * T * d * 2 + T * K * 8
-    gateup = {"flops": 2 * rows * d * I * 2, "bytes": n_touched * 2 * I * d * 2 + rows * d * 2 + rows * I * 2}
-    down = {"flops": 2 * rows * I * d, "bytes": n_touched * d * I * 2 + rows * I * 2 + rows * d * 4}
-    return layer_flops, layer_bytes, {"gateup_gemm": gateup, "down_gemm": down}
+    # weights once; x_perm read, h written and read back, y written
+    mlp = {"flops": 2 * rows * d * I * 3,
+           "bytes": n_touched * 3 * I * d * 2 + rows * d * 2 + 2 * rows * I * 2 + rows * d * 4}
+    return layer_flops, layer_bytes, {"expert_mlp": mlp}
 
 
 def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=True):
@@ -193,7 +196,7 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     layer_flops, layer_bytes, kern = algorithmic(shape, T, n_touched, rows)
     t_roof_s = max(layer_flops / (pk["bf16_tflops"] * 1e12), layer_bytes / (pk["hbm_gbs"] * 1e9))
     ms_per_step = total_ms / steps
-    dom = max(("gateup_gemm", "down_gemm"), key=lambda k: stage_ms[k])
+    dom = "expert_mlp"
     kf, kb = kern[dom]["flops"], kern[dom]["bytes"]
     t_dom = stage_ms[dom] * 1e-3
     hbm_bound = kb / (pk["hbm_gbs"] * 1e9) >= kf / (pk["bf16_tflops"] * 1e12)
@@ -206,7 +209,7 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
     roof["kernel_ms"] = stage_ms[dom]
     tr = TRAFFIC.get(name)
-    roof["traffic"] = tr["bytes"] if tr and tr.get("kernel") == dom else None
+    roof["traffic"] = tr["bytes_per_touched_expert"] * n_touched if tr and tr.get("kernel") == dom else None
 
     res = {
         "value": T * steps / (total_ms * 1e-3),

@@ -178,9 +178,9 @@ BEAM_MOE_API int beam_moe_device_status(cudaStream_t stream);
  * records CUDA events on its stream around each stage; beam_moe_timing_read synchronises
  * on the last call's final event and writes up to max_stages durations in milliseconds
  * (stage order: pre-norm, router weight split, router logits, router select, dispatch count,
- * dispatch scan, dispatch scatter, gather, gate/up GEMM, down GEMM, combine (fused with the
- * post-norm and residual in beam_moe_sublayer_forward); unrun stages read 0). Returns the
- * number of stages, or a negative error. */
+ * dispatch scan, dispatch scatter, gather, expert MLP (gate/up, SwiGLU and down in one
+ * kernel), combine (fused with the post-norm and residual in beam_moe_sublayer_forward);
+ * unrun stages read 0). Returns the number of stages, or a negative error. */
 BEAM_MOE_API int beam_moe_timing_enable(int enable);
 BEAM_MOE_API int beam_moe_timing_read(float *ms, int max_stages);
 

@@ -76,7 +76,7 @@ int check_stream(cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------- stage timing
-enum Stage { kPreNorm, kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kGateUp, kDown, kCombine, kNumStages };
+enum Stage { kPreNorm, kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kExpert, kCombine, kNumStages };
 struct Timing {
     bool enabled = false;
     bool created = false;
@@ -140,6 +140,7 @@ struct Scratch {
     int* chunk = nullptr;
     int* expert_offset = nullptr;
     int4* tiles = nullptr;
+    int* tile_done = nullptr;
     int* perm_src = nullptr;
     int* inv_slot = nullptr;
     bf16* x_perm = nullptr;
@@ -176,6 +177,7 @@ size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool
         sc->chunk = c.take<int>(static_cast<size_t>(nchunks) * s.E);
         sc->expert_offset = c.take<int>(s.E + 1);
         sc->tiles = c.take<int4>(1 + static_cast<size_t>(max_tiles));
+        sc->tile_done = c.take<int>(static_cast<size_t>(max_tiles));
         sc->perm_src = c.take<int>(pairs);
         sc->inv_slot = c.take<int>(pairs);
         sc->x_perm = c.take<bf16>(pairs * s.d);
@@ -279,13 +281,11 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
                                              mode == 1 ? logits : nullptr, st));
         if (fwd) {
             LAUNCH(kCount, launch_dispatch_count(s, idx, T, sc.chunk, dev->status, st));
-            LAUNCH(kScan, launch_dispatch_scan(s, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, st));
+            LAUNCH(kScan, launch_dispatch_scan(s, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, sc.tile_done, st));
             LAUNCH(kScatter, launch_dispatch_scatter(s, idx, T, sc.chunk, sc.perm_src, sc.inv_slot, dev->status, st));
             LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, rows, sc.x_perm, dev->status, dev->num_sms, st));
-            LAUNCH(kGateUp, launch_gateup(s, wg, wu, sc.x_perm, rows, sc.tiles, max_tiles, bn_max, sc.h, dev->status,
-                                          dev->num_sms, st));
-            LAUNCH(kDown, launch_down(s, wd, sc.h, rows, sc.tiles, max_tiles, bn_max, sc.y, dev->status,
-                                      dev->num_sms, st));
+            LAUNCH(kExpert, launch_expert_mlp(s, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
+                                              bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
             if (mode == 3)
                 LAUNCH(kCombine, launch_combine_residual(s, sc.y, sc.inv_slot, w, T, stream_in, sub->post_gamma,
                                                          sub->eps, sub->k, out, dev->status, st));

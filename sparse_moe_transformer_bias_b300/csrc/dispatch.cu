@@ -8,7 +8,8 @@
 //   count:   per-chunk expert histogram from the bitmap;
 //   scan:    per expert, exclusive scan over chunks; then an exclusive scan over experts
 //            gives each expert's first permuted row; also emits the GEMM work list of
-//            N-tiles (at most bn_max rows each, split evenly);
+//            N-tiles (at most bn_max rows each, split evenly), with the header's item
+//            counter and every tile's completion counter set to zero;
 //   scatter: permuted row of (t, k) = chunk base of e + rank; writes perm_src[row] = t
 //            and inv_slot[t, k] = row;
 //   gather:  x_perm[row] = x[perm_src[row]] with 16-byte loads and stores.
@@ -55,7 +56,8 @@ __global__ void __launch_bounds__(kChunk) dispatch_count_kernel(const int32_t* _
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int nchunks, int E, int bn_max,
                                                              int* __restrict__ chunk_count,
                                                              int* __restrict__ expert_offset,
-                                                             int4* __restrict__ tiles) {
+                                                             int4* __restrict__ tiles,
+                                                             int* __restrict__ tile_done) {
     __shared__ int tot[1024];
     __shared__ int ntl[1024];
     const int e = threadIdx.x;
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int nchunks, int E,
             int tile = ntl[e] - nt;
             for (int r = 0; r < n; r += per) {
                 const int rows = min(per, n - r);
+                if (tile_done) tile_done[tile] = 0;
                 tiles[1 + tile++] = make_int4(e, base + r, rows, 0);
             }
         }
@@ -166,9 +169,9 @@ cudaError_t launch_dispatch_count(const Shape& s, const int32_t* topk_idx, int T
 }
 
 cudaError_t launch_dispatch_scan(const Shape& s, int T, int bn_max, int* chunk_count, int* expert_offset, int4* tiles,
-                                 cudaStream_t st) {
+                                 int* tile_done, cudaStream_t st) {
     const int nchunks = (T + kChunk - 1) / kChunk;
-    dispatch_scan_kernel<<<1, 1024, 0, st>>>(nchunks, s.E, bn_max, chunk_count, expert_offset, tiles);
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(nchunks, s.E, bn_max, chunk_count, expert_offset, tiles, tile_done);
     return cudaGetLastError();
 }
 

@@ -46,27 +46,28 @@ int dispatch_max_tiles(const Shape& s, int T, int bn_max);
 cudaError_t launch_dispatch_count(const Shape& s, const int32_t* topk_idx, int T, int* chunk_count, int* status,
                                   cudaStream_t st);
 cudaError_t launch_dispatch_scan(const Shape& s, int T, int bn_max, int* chunk_count, int* expert_offset,
-                                 int4* tiles, cudaStream_t st);
+                                 int4* tiles, int* tile_done, cudaStream_t st);
 cudaError_t launch_dispatch_scatter(const Shape& s, const int32_t* topk_idx, int T, const int* chunk_base,
                                     int* perm_src, int* inv_slot, int* status, cudaStream_t st);
 cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, int rows, bf16* x_perm,
                                int* status, int num_sms, cudaStream_t st);
 
-// ---------------------------------------------------------------- grouped GEMMs (grouped_gemm.cu)
-// Largest N-tile (tokens per tile) the GEMMs use for a batch of T tokens.
+// ---------------------------------------------------------------- expert MLP (expert_mlp.cu)
+// Largest N-tile (token rows per tile) the expert kernel uses for a batch of T tokens.
 int gemm_bn_max(const Shape& s, int T);
-// h[rows, I] = silu(x_perm . Wg[e]^T) * (x_perm . Wu[e]^T), per N-tile of the work list.
-cudaError_t launch_gateup(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* x_perm, int rows,
-                          const int4* tiles, int max_tiles, int bn_max, bf16* h, int* status, int num_sms,
-                          cudaStream_t st);
+// Both expert products in one persistent kernel (expert_mlp.cu): h = SwiGLU(x_perm) and
+// y = h . Wd^T per N-tile of the work list, scheduled dynamically; tile_done[max_tiles]
+// and the work list's item counter must be zero (dispatch_scan sets them).
+cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* w_down,
+                              const bf16* x_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
+                              int bn_max, bf16* h, float* y, int* status, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- router product (router_gemm.cu)
 // Split-K count of the tensor-core router product for T tokens.
 int router_tc_splits(const Shape& s, int T, int num_sms);
 // partial[split][t][e] = sum over the split's K range of x[t] . (hi + mid + lo)[e].
 cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int T, int splits, float* partial,
                              int* status, int num_sms, cudaStream_t st);
-// y[rows, d] = h . Wd[e]^T (FP32), per N-tile of the work list.
-cudaError_t launch_down(const Shape& s, const bf16* w_down, const bf16* h, int rows, const int4* tiles, int max_tiles,
-                        int bn_max, float* y, int* status, int num_sms, cudaStream_t st);
 
 // ---------------------------------------------------------------- combine (combine.cu)
 cudaError_t launch_combine(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T, bf16* out,
@@ -91,6 +92,21 @@ cudaError_t launch_rmsnorm(int d, const bf16* v, const bf16* gamma, float eps, i
 cudaError_t launch_combine_residual(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T,
                                     const bf16* stream_in, const bf16* gamma, float eps, int k_contrib,
                                     bf16* stream_out, int* status, cudaStream_t st);
+
+// ---------------------------------------------------------------- tcgen05 GEMM tiling (shared)
+constexpr int kTileM = 128;    // weight rows per tile (MMA M)
+constexpr int kTileK = 64;     // K per pipeline stage: one 128-byte swizzle row of BF16
+constexpr int kMmaK = 16;      // K per tcgen05.mma (kind::f16)
+constexpr int kBoxRows = 16;   // granule of token rows (MMA N step, smallest TMA box)
+constexpr int kBoxKinds = 5;   // token-row tensor maps with boxes of 16, 32, 64, 128, 256 rows
+
+// A BF16 [rows, cols] token-row operand as tensor maps that differ only in box height:
+// m[i] has boxes of (16 << i) rows x 64 columns (128-byte swizzle).
+struct BMaps {
+    CUtensorMap m[kBoxKinds];
+};
+// Encodes the maps for every box height up to bn_max (larger ones repeat m[0]).
+bool encode_bmaps(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int bn_max, const char** why);
 
 // Host helper: encode a 2-D BF16 tensor map (rows x cols, row-major) with the 128-byte
 // swizzle and a box of box_cols x box_rows. Returns false if the driver refuses it.

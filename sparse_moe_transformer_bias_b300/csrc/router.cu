@@ -5,7 +5,7 @@
 // Stage 1: FP32 logits l = x . Wr^T (x is exactly BF16).
 //   T <= 32 (decode): router_logits_small_kernel on CUDA cores, FP32 fused multiply-adds,
 //   one CTA per two experts over the whole K, reduced in a fixed order.
-//   T > 32: the tensor-core product of grouped_gemm.cu in router mode, after
+//   T > 32: the tensor-core product of router_gemm.cu, after
 //   router_split_weights_kernel has written Wr as three BF16 pieces hi + mid + lo == Wr
 //   (exactly); the products x.piece are exact and accumulate in FP32. Split-K partial
 //   planes are added in split order by stage 2, so the result is deterministic.
@@ -24,12 +24,14 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // Small batches (T <= kSmallT, decode): one CTA per kSmallEPB experts computes their logits
 // for every token over the whole K, so no split-K partials are written. Warp w sums the
-// K range [w*d/8, (w+1)*d/8) with lane-strided 4-wide FMAs in ascending K; the 32 lanes
-// are combined by a fixed butterfly and the 8 warps in warp order, so the result is
-// deterministic.
+// K range [w*d/8, (w+1)*d/8): each lane first loads its 4-wide slices of the experts'
+// weights for the whole range (all loads in flight at once), then streams the tokens,
+// FMA-ing in ascending K. The 32 lanes are combined by a fixed butterfly and the 8 warps
+// in warp order, so the result is deterministic.
 constexpr int kSmallT = 32;
 constexpr int kSmallEPB = 2;
 constexpr int kSmallWarps = 8;
+constexpr int kSmallMaxIt = 8;  // 128-wide K steps per warp: d <= 8 * 128 * 8
 
 __global__ void __launch_bounds__(kSmallWarps * 32) router_logits_small_kernel(const bf16* __restrict__ x,
                                                                               const float* __restrict__ wr, int T,
@@ -39,33 +41,39 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_logits_small_kernel(c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * kSmallEPB;
     const int kw = d / kSmallWarps;
-    const int kbeg = warp * kw, kend = kbeg + kw;
-    float acc[kSmallT][kSmallEPB];
+    const int kbeg = warp * kw + 4 * lane, kend = (warp + 1) * kw;
+    float4 w[kSmallMaxIt][kSmallEPB];
 #pragma unroll
-    for (int t = 0; t < kSmallT; ++t)
-#pragma unroll
-        for (int j = 0; j < kSmallEPB; ++j) acc[t][j] = 0.f;
-    for (int k = kbeg + 4 * lane; k < kend; k += 128) {
-        float4 w[kSmallEPB];
+    for (int it = 0; it < kSmallMaxIt; ++it) {
+        const int k = kbeg + 128 * it;
 #pragma unroll
         for (int j = 0; j < kSmallEPB; ++j)
-            w[j] = (e0 + j < E) ? *reinterpret_cast<const float4*>(wr + static_cast<size_t>(e0 + j) * d + k)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            w[it][j] = (k < kend && e0 + j < E) ? *reinterpret_cast<const float4*>(wr + static_cast<size_t>(e0 + j) * d + k)
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float acc[kSmallT][kSmallEPB];
 #pragma unroll
-        for (int t = 0; t < kSmallT; ++t) {
-            if (t < T) {
-                const uint2 raw = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * d + k);
-                const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-                const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-                const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    for (int t = 0; t < kSmallT; ++t) {
 #pragma unroll
-                for (int j = 0; j < kSmallEPB; ++j) {
-                    float v = acc[t][j];
-                    v = fmaf(a.x, w[j].x, v);
-                    v = fmaf(a.y, w[j].y, v);
-                    v = fmaf(b.x, w[j].z, v);
-                    v = fmaf(b.y, w[j].w, v);
-                    acc[t][j] = v;
+        for (int j = 0; j < kSmallEPB; ++j) acc[t][j] = 0.f;
+        if (t < T) {
+#pragma unroll
+            for (int it = 0; it < kSmallMaxIt; ++it) {
+                const int k = kbeg + 128 * it;
+                if (k < kend) {
+                    const uint2 raw = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * d + k);
+                    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+                    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+                    const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+#pragma unroll
+                    for (int j = 0; j < kSmallEPB; ++j) {
+                        float v = acc[t][j];
+                        v = fmaf(a.x, w[it][j].x, v);
+                        v = fmaf(a.y, w[it][j].y, v);
+                        v = fmaf(b.x, w[it][j].z, v);
+                        v = fmaf(b.y, w[it][j].w, v);
+                        acc[t][j] = v;
+                    }
                 }
             }
         }
@@ -86,7 +94,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_logits_small_kernel(c
         if (e0 + j >= E) continue;
         float v = red[0][i];
 #pragma unroll
-        for (int w = 1; w < kSmallWarps; ++w) v += red[w][i];
+        for (int w8 = 1; w8 < kSmallWarps; ++w8) v += red[w8][i];
         logits[static_cast<size_t>(t) * E + e0 + j] = v;
     }
 }
@@ -223,7 +231,7 @@ __global__ void __launch_bounds__(256) router_split_weights_kernel(const float4*
 
 RouterPlan router_plan(const Shape& s, int T, int num_sms) {
     RouterPlan p;
-    if (T <= kSmallT) {
+    if (T <= kSmallT && s.d <= kSmallWarps * 128 * kSmallMaxIt) {
         p.tensor = false;
         p.splits = 1;
         p.w3_elems = 0;

@@ -1,0 +1,64 @@
+// Host helpers for the TMA tensor maps of the tcgen05 kernels (router_gemm.cu,
+// expert_mlp.cu): BF16 row-major matrices, 128-byte swizzle, boxes of 64 columns.
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace beam {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's encoder, fetched through the runtime once (the library does not link libcuda).
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                         uint32_t box_cols, const char** why) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        *why = "driver entry point cuTensorMapEncodeTiled is not available";
+        return false;
+    }
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *why = "cuTensorMapEncodeTiled rejected a tensor map";
+        return false;
+    }
+    return true;
+}
+
+bool encode_bmaps(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int bn_max, const char** why) {
+    for (int i = 0; i < kBoxKinds; ++i) {
+        const uint32_t h = kBoxRows << i;
+        if (static_cast<int>(h) > bn_max) {
+            b->m[i] = b->m[0];
+            continue;
+        }
+        if (!encode_tmap_bf16_2d(&b->m[i], base, rows, cols, h, kTileK, why)) return false;
+    }
+    return true;
+}
+
+}  // namespace beam
