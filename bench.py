@@ -287,7 +287,8 @@ def barrier():
 
 def max_over_ranks(v):
     if torch.distributed.is_available() and torch.distributed.is_initialized():
-        t = torch.tensor([float(v)], device="cuda")
+        dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([float(v)], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         return float(t.item())
     return float(v)

@@ -110,6 +110,22 @@ BEAM_MOE_API int beam_moe_forward_ex(const beam_moe_config *cfg, const __nv_bflo
                         const float *expert_bias, const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up,
                         const __nv_bfloat16 *w_down, int T, __nv_bfloat16 *out, cudaStream_t stream);
 
+/* One expert-parallel shard of the MoE block. The pages' multi-GPU plan puts each expert on
+ * one device and replicates the rest, with a device count that divides 256 (Glonce "Reflection
+ * releases Beam ...", Running it paragraph; transformers "Beam" doc, Usage examples: expert
+ * parallelism with torchrun). The calling device holds experts [e_begin, e_end) only:
+ *   w_gate, w_up  bf16 [e_end - e_begin, I, d];  w_down  bf16 [e_end - e_begin, d, I]
+ * Routing runs over all E experts (router_w and expert_bias are the full, replicated ones);
+ * the call runs the (token, slot) pairs routed to its experts and writes
+ *   out_partial[t] = sum over slots k with e_k in [e_begin, e_end) of w_k * SwiGLU_{e_k}(x[t])
+ * FP32 [T, d], not rounded (slots in order). The sum of out_partial over shards that cover
+ * [0, E) is the block's output before its rounding to BF16: the combine of expert
+ * parallelism is a sum over devices (an all-reduce). Tokens with no slot on this shard get 0. */
+BEAM_MOE_API int beam_moe_forward_shard(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
+                           const float *expert_bias, const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up,
+                           const __nv_bfloat16 *w_down, int e_begin, int e_end, int T, float *out_partial,
+                           cudaStream_t stream);
+
 /* Pre-norm of the MoE sublayer (transformers "Beam" doc, Overview, "Sandwich norms with
  * depth-scaled residuals" bullet: each block is wrapped in an RMSNorm before and after;
  * the paragraph after the bullets: RMSNorm scaling is computed in FP32):

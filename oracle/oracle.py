@@ -230,6 +230,25 @@ class Oracle:
         return out, x_rows
 
 
+    def forward_shard(self, shape, x_bits, bias, experts, e_begin, e_end, tokens, logits=None, router_w=None):
+        """One expert-parallel shard's partial output for the rows `tokens`: the sum over the
+        token's slots routed to experts [e_begin, e_end) of w_k * expert_k(x), FP64, with
+        the oracle's own routing (from `logits` if given, else from router_w).
+        experts: callable e -> (wg_e, wu_e, wd_e) bit patterns for the shard's experts."""
+        x_bits = _u16(x_bits)
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        lg = _f32(logits)[tokens] if logits is not None else self.router_logits(shape, x_bits[tokens], router_w)
+        idx, _, dbg = self.route(shape, lg, bias, debug=True)
+        out = np.zeros((len(tokens), shape.d), np.float64)
+        for n, t in enumerate(tokens):
+            xr = (x_bits[t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            for k in range(shape.top_k):
+                e = int(idx[n, k])
+                if e_begin <= e < e_end:
+                    out[n] += dbg["w64"][n, k] * self.expert(shape, xr, *experts(e))
+        return out
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -268,6 +287,10 @@ def round_bf16(*a, **k):
 
 def sublayer(*a, **k):
     return default().sublayer(*a, **k)
+
+
+def forward_shard(*a, **k):
+    return default().forward_shard(*a, **k)
 
 
 def bf16_bits(t) -> np.ndarray:

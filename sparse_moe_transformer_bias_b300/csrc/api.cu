@@ -206,12 +206,19 @@ struct SublayerArgs {
     int k;
 };
 
+// An expert-parallel shard's extra inputs (mode 4): its experts and its FP32 output.
+struct ShardArgs {
+    int e_begin, e_end;
+    float* out_partial;
+};
+
 // mode 0: route (outputs topk_idx/topk_w); 1: logits only; 2: forward; 3: sublayer (x is
 // the residual stream: pre-norm, forward, then combine fused with the post-norm and the
-// residual update into out).
+// residual update into out); 4: forward of one expert-parallel shard (wg/wu/wd hold only
+// experts [e_begin, e_end); FP32 partial output over the slots routed there).
 int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float* bias, const bf16* wg,
         const bf16* wu, const bf16* wd, int T, int32_t* topk_idx, float* topk_w, float* logits, bf16* out, int mode,
-        cudaStream_t st, const SublayerArgs* sub = nullptr) {
+        cudaStream_t st, const SublayerArgs* sub = nullptr, const ShardArgs* shard = nullptr) {
     g_launches = 0;
     timing_begin_call();
     int rc;
@@ -227,9 +234,16 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     if (mode != 1 && (rc = check_ptr(bias, "expert_bias"))) return rc;
     if (mode == 0 && ((rc = check_ptr(topk_idx, "topk_idx")) || (rc = check_ptr(topk_w, "topk_w")))) return rc;
     if (mode == 1 && (rc = check_ptr(logits, "logits"))) return rc;
-    if (mode >= 2 && ((rc = check_ptr(wg, "w_gate")) || (rc = check_ptr(wu, "w_up")) ||
-                      (rc = check_ptr(wd, "w_down")) || (rc = check_ptr(out, mode == 3 ? "stream_out" : "out"))))
+    if (mode >= 2 && ((rc = check_ptr(wg, "w_gate")) || (rc = check_ptr(wu, "w_up")) || (rc = check_ptr(wd, "w_down"))))
         return rc;
+    if (mode == 4) {
+        if ((rc = check_ptr(shard->out_partial, "out_partial"))) return rc;
+        if (shard->e_begin < 0 || shard->e_begin >= shard->e_end || shard->e_end > cfg->E)
+            return fail(BEAM_MOE_ERR_ARG, "expert range [%d, %d) must be a non-empty part of [0, %d)", shard->e_begin,
+                        shard->e_end, cfg->E);
+    } else if (mode >= 2 && (rc = check_ptr(out, mode == 3 ? "stream_out" : "out"))) {
+        return rc;
+    }
     if (T == 0) return BEAM_MOE_OK;
     if ((rc = check_stream(st))) return rc;
     DeviceState* dev = nullptr;
@@ -256,9 +270,13 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     }
 
     const Shape s = shape_of(cfg);
+    // The experts this call runs: all of them, or the shard's (local ids from 0).
+    const int e_lo = mode == 4 ? shard->e_begin : 0;
+    Shape se = s;
+    se.E = mode == 4 ? shard->e_end - shard->e_begin : s.E;
     const RouterPlan plan = router_plan(s, T, dev->num_sms);
     const int bn_max = gemm_bn_max(s, T);
-    const int max_tiles = dispatch_max_tiles(s, T, bn_max);
+    const int max_tiles = dispatch_max_tiles(se, T, bn_max);
     const int rows = T * s.top_k;
     Scratch sc;
     const bool fwd = mode >= 2;
@@ -280,13 +298,18 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
         LAUNCH(kSelect, launch_router_select(s, sc.partial, plan.splits, mode == 1 ? nullptr : bias, T, idx, w,
                                              mode == 1 ? logits : nullptr, st));
         if (fwd) {
-            LAUNCH(kCount, launch_dispatch_count(s, idx, T, sc.chunk, dev->status, st));
-            LAUNCH(kScan, launch_dispatch_scan(s, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, sc.tile_done, st));
-            LAUNCH(kScatter, launch_dispatch_scatter(s, idx, T, sc.chunk, sc.perm_src, sc.inv_slot, dev->status, st));
-            LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, rows, sc.x_perm, dev->status, dev->num_sms, st));
-            LAUNCH(kExpert, launch_expert_mlp(s, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
+            LAUNCH(kCount, launch_dispatch_count(s, e_lo, se.E, idx, T, sc.chunk, dev->status, st));
+            LAUNCH(kScan, launch_dispatch_scan(se.E, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, sc.tile_done, st));
+            LAUNCH(kScatter, launch_dispatch_scatter(s, e_lo, se.E, idx, T, sc.chunk, sc.perm_src, sc.inv_slot,
+                                                     dev->status, st));
+            LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
+                                               dev->status, dev->num_sms, st));
+            LAUNCH(kExpert, launch_expert_mlp(se, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
                                               bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
-            if (mode == 3)
+            if (mode == 4)
+                LAUNCH(kCombine, launch_combine_partial(s, sc.y, sc.inv_slot, w, T, shard->out_partial, dev->status,
+                                                        st));
+            else if (mode == 3)
                 LAUNCH(kCombine, launch_combine_residual(s, sc.y, sc.inv_slot, w, T, stream_in, sub->post_gamma,
                                                          sub->eps, sub->k, out, dev->status, st));
             else
@@ -365,6 +388,15 @@ int beam_moe_sublayer_forward(const beam_moe_config* cfg, const __nv_bfloat16* s
     const SublayerArgs sub{pre_gamma, post_gamma, eps, k};
     return run(cfg, stream_in, router_w, expert_bias, w_gate, w_up, w_down, T, nullptr, nullptr, nullptr, stream_out, 3,
                stream, &sub);
+}
+
+int beam_moe_forward_shard(const beam_moe_config* cfg, const __nv_bfloat16* x, const float* router_w,
+                           const float* expert_bias, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
+                           const __nv_bfloat16* w_down, int e_begin, int e_end, int T, float* out_partial,
+                           cudaStream_t stream) {
+    const ShardArgs sh{e_begin, e_end, out_partial};
+    return run(cfg, x, router_w, expert_bias, w_gate, w_up, w_down, T, nullptr, nullptr, nullptr, nullptr, 4, stream,
+               nullptr, &sh);
 }
 
 int beam_moe_rmsnorm(int d, const __nv_bfloat16* v, const __nv_bfloat16* gamma, float eps, int T,

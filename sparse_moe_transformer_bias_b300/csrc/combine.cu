@@ -3,21 +3,27 @@
 // already inside the weights): out[t] = sum_k w[t,k] * y[inv_slot[t,k]], FP32 fused
 // multiply-adds in slot order k = 0..top_k-1 (a gather, so the order is fixed and the
 // result deterministic), rounded once to BF16. 16-byte loads of y, 8-byte stores of out.
+// Shard mode (expert parallelism): slots routed to another shard (inv_slot = -1) are left
+// out and the FP32 partial sum is stored unrounded, for the sum over shards.
 #include "internal.cuh"
 
 namespace beam {
 namespace {
 
+template <bool kPartial>
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y, const int* __restrict__ inv_slot,
                                                       const float* __restrict__ topk_w, int K, int d4, int n_rows,
-                                                      uint2* __restrict__ out, int* status) {
+                                                      void* __restrict__ out, int* status) {
     const int t = blockIdx.x;
     __shared__ int rows[32];
     __shared__ float ws[32];
     if (threadIdx.x < K) {
         int r = inv_slot[static_cast<size_t>(t) * K + threadIdx.x];
         float w = topk_w[static_cast<size_t>(t) * K + threadIdx.x];
-        if (static_cast<unsigned>(r) >= static_cast<unsigned>(n_rows)) {
+        if (kPartial && r < 0) {  // another shard's expert
+            r = 0;
+            w = 0.f;
+        } else if (static_cast<unsigned>(r) >= static_cast<unsigned>(n_rows)) {
             atomicCAS(status, 0, kStatusBadIndex);
             r = 0;
             w = 0.f;
@@ -29,19 +35,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
     for (int c = blockIdx.y * blockDim.x + threadIdx.x; c < d4; c += gridDim.y * blockDim.x) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < K; ++k) {
-            const float4 v = y[static_cast<size_t>(rows[k]) * d4 + c];
             const float w = ws[k];
+            if (kPartial && w == 0.f) continue;
+            const float4 v = y[static_cast<size_t>(rows[k]) * d4 + c];
             acc.x = fmaf(w, v.x, acc.x);
             acc.y = fmaf(w, v.y, acc.y);
             acc.z = fmaf(w, v.z, acc.z);
             acc.w = fmaf(w, v.w, acc.w);
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&lo);
-        o.y = *reinterpret_cast<uint32_t*>(&hi);
-        out[static_cast<size_t>(t) * d4 + c] = o;
+        if constexpr (kPartial) {
+            static_cast<float4*>(out)[static_cast<size_t>(t) * d4 + c] = acc;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 o;
+            o.x = *reinterpret_cast<uint32_t*>(&lo);
+            o.y = *reinterpret_cast<uint32_t*>(&hi);
+            static_cast<uint2*>(out)[static_cast<size_t>(t) * d4 + c] = o;
+        }
     }
 }
 
@@ -54,8 +65,19 @@ cudaError_t launch_combine(const Shape& s, const float* y, const int* inv_slot, 
     int ysplit = 1;
     while (T * ysplit < 296 && ysplit * 256 * 2 <= d4) ysplit *= 2;
     const dim3 grid(T, ysplit);
-    combine_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
-                                         T * s.top_k, reinterpret_cast<uint2*>(out), status);
+    combine_kernel<false><<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
+                                                T * s.top_k, out, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_partial(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T,
+                                   float* out, int* status, cudaStream_t st) {
+    const int d4 = s.d / 4;
+    int ysplit = 1;
+    while (T * ysplit < 296 && ysplit * 256 * 2 <= d4) ysplit *= 2;
+    const dim3 grid(T, ysplit);
+    combine_kernel<true><<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
+                                               T * s.top_k, out, status);
     return cudaGetLastError();
 }
 

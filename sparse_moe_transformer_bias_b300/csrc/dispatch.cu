@@ -21,8 +21,10 @@ namespace {
 constexpr int kChunk = kDispatchChunk;
 constexpr int kWords = kChunk / 32;
 
-__device__ __forceinline__ void build_bitmap(uint32_t* bm, const int32_t* __restrict__ idx, int T, int E, int K,
-                                             int t0, int* status) {
+// Experts [e_lo, e_lo + E) are this call's (all of them, or one expert-parallel shard);
+// pairs routed elsewhere are left out. Bitmap rows are local expert ids.
+__device__ __forceinline__ void build_bitmap(uint32_t* bm, const int32_t* __restrict__ idx, int T, int E_all,
+                                             int e_lo, int E, int K, int t0, int* status) {
     for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) bm[i] = 0u;
     __syncthreads();
     const int tl = threadIdx.x;
@@ -30,20 +32,23 @@ __device__ __forceinline__ void build_bitmap(uint32_t* bm, const int32_t* __rest
     if (t < T) {
         for (int k = 0; k < K; ++k) {
             const int e = idx[static_cast<size_t>(t) * K + k];
-            if (e < 0 || e >= E) {
+            if (e < 0 || e >= E_all) {
                 atomicCAS(status, 0, kStatusBadExpert);
                 continue;
             }
-            atomicOr(&bm[e * kWords + (tl >> 5)], 1u << (tl & 31));
+            const int el = e - e_lo;
+            if (el < 0 || el >= E) continue;
+            atomicOr(&bm[el * kWords + (tl >> 5)], 1u << (tl & 31));
         }
     }
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kChunk) dispatch_count_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
+__global__ void __launch_bounds__(kChunk) dispatch_count_kernel(const int32_t* __restrict__ idx, int T, int E_all,
+                                                                int e_lo, int E, int K,
                                                                 int* __restrict__ chunk_count, int* status) {
     extern __shared__ uint32_t bm[];
-    build_bitmap(bm, idx, T, E, K, blockIdx.x * kChunk, status);
+    build_bitmap(bm, idx, T, E_all, e_lo, E, K, blockIdx.x * kChunk, status);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int n = 0;
 #pragma unroll
@@ -108,24 +113,28 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int nchunks, int E,
     }
 }
 
-__global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(const int32_t* __restrict__ idx, int T, int E,
-                                                                  int K, const int* __restrict__ chunk_base,
+__global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(const int32_t* __restrict__ idx, int T, int E_all,
+                                                                  int e_lo, int E, int K,
+                                                                  const int* __restrict__ chunk_base,
                                                                   int* __restrict__ perm_src,
                                                                   int* __restrict__ inv_slot, int* status) {
     extern __shared__ uint32_t bm[];
     const int t0 = blockIdx.x * kChunk;
-    build_bitmap(bm, idx, T, E, K, t0, status);
+    build_bitmap(bm, idx, T, E_all, e_lo, E, K, t0, status);
     const int tl = threadIdx.x;
     const int t = t0 + tl;
     if (t >= T) return;
     const int w = tl >> 5;
     const uint32_t below = (1u << (tl & 31)) - 1u;
     for (int k = 0; k < K; ++k) {
-        const int e = idx[static_cast<size_t>(t) * K + k];
-        if (e < 0 || e >= E) continue;
-        int rank = __popc(bm[e * kWords + w] & below);
-        for (int j = 0; j < w; ++j) rank += __popc(bm[e * kWords + j]);
-        const int row = chunk_base[static_cast<size_t>(blockIdx.x) * E + e] + rank;
+        const int el = idx[static_cast<size_t>(t) * K + k] - e_lo;
+        if (el < 0 || el >= E) {  // routed to another shard (or invalid, already flagged)
+            inv_slot[static_cast<size_t>(t) * K + k] = -1;
+            continue;
+        }
+        int rank = __popc(bm[el * kWords + w] & below);
+        for (int j = 0; j < w; ++j) rank += __popc(bm[el * kWords + j]);
+        const int row = chunk_base[static_cast<size_t>(blockIdx.x) * E + el] + rank;
         if (row < 0 || row >= T * K) {
             atomicCAS(status, 0, kStatusBadIndex);
             continue;
@@ -136,9 +145,10 @@ __global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(const int32_t*
 }
 
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int row_vecs, int T,
-                                                          const int* __restrict__ perm_src, int rows,
+                                                          const int* __restrict__ perm_src,
+                                                          const int* __restrict__ n_rows,
                                                           uint4* __restrict__ x_perm, int* status) {
-    const size_t total = static_cast<size_t>(rows) * row_vecs;
+    const size_t total = static_cast<size_t>(*n_rows) * row_vecs;  // rows this call dispatched
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const size_t r = i / row_vecs;
@@ -160,32 +170,32 @@ int dispatch_max_tiles(const Shape& s, int T, int bn_max) {
     return static_cast<int>(pairs / bn_max + used + 1);
 }
 
-cudaError_t launch_dispatch_count(const Shape& s, const int32_t* topk_idx, int T, int* chunk_count, int* status,
-                                  cudaStream_t st) {
+cudaError_t launch_dispatch_count(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T, int* chunk_count,
+                                  int* status, cudaStream_t st) {
     const int nchunks = (T + kChunk - 1) / kChunk;
-    const size_t smem = static_cast<size_t>(s.E) * kWords * sizeof(uint32_t);
-    dispatch_count_kernel<<<nchunks, kChunk, smem, st>>>(topk_idx, T, s.E, s.top_k, chunk_count, status);
+    const size_t smem = static_cast<size_t>(E_loc) * kWords * sizeof(uint32_t);
+    dispatch_count_kernel<<<nchunks, kChunk, smem, st>>>(topk_idx, T, s.E, e_lo, E_loc, s.top_k, chunk_count, status);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dispatch_scan(const Shape& s, int T, int bn_max, int* chunk_count, int* expert_offset, int4* tiles,
+cudaError_t launch_dispatch_scan(int E_loc, int T, int bn_max, int* chunk_count, int* expert_offset, int4* tiles,
                                  int* tile_done, cudaStream_t st) {
     const int nchunks = (T + kChunk - 1) / kChunk;
-    dispatch_scan_kernel<<<1, 1024, 0, st>>>(nchunks, s.E, bn_max, chunk_count, expert_offset, tiles, tile_done);
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(nchunks, E_loc, bn_max, chunk_count, expert_offset, tiles, tile_done);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dispatch_scatter(const Shape& s, const int32_t* topk_idx, int T, const int* chunk_base,
-                                    int* perm_src, int* inv_slot, int* status, cudaStream_t st) {
+cudaError_t launch_dispatch_scatter(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T,
+                                    const int* chunk_base, int* perm_src, int* inv_slot, int* status, cudaStream_t st) {
     const int nchunks = (T + kChunk - 1) / kChunk;
-    const size_t smem = static_cast<size_t>(s.E) * kWords * sizeof(uint32_t);
-    dispatch_scatter_kernel<<<nchunks, kChunk, smem, st>>>(topk_idx, T, s.E, s.top_k, chunk_base, perm_src, inv_slot,
-                                                           status);
+    const size_t smem = static_cast<size_t>(E_loc) * kWords * sizeof(uint32_t);
+    dispatch_scatter_kernel<<<nchunks, kChunk, smem, st>>>(topk_idx, T, s.E, e_lo, E_loc, s.top_k, chunk_base, perm_src,
+                                                           inv_slot, status);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, int rows, bf16* x_perm,
-                               int* status, int num_sms, cudaStream_t st) {
+cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, const int* n_rows, int rows,
+                               bf16* x_perm, int* status, int num_sms, cudaStream_t st) {
     const int row_vecs = d / 8;
     const long long total = static_cast<long long>(rows) * row_vecs;
     long long blocks = (total + 255) / 256;
@@ -193,7 +203,7 @@ cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src,
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const uint4*>(x), row_vecs, T,
-                                                                      perm_src, rows,
+                                                                      perm_src, n_rows,
                                                                       reinterpret_cast<uint4*>(x_perm), status);
     return cudaGetLastError();
 }

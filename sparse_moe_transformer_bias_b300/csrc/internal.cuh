@@ -43,14 +43,18 @@ cudaError_t launch_router_select(const Shape& s, const float* partial, int split
 
 // ---------------------------------------------------------------- dispatch (dispatch.cu)
 int dispatch_max_tiles(const Shape& s, int T, int bn_max);
-cudaError_t launch_dispatch_count(const Shape& s, const int32_t* topk_idx, int T, int* chunk_count, int* status,
-                                  cudaStream_t st);
-cudaError_t launch_dispatch_scan(const Shape& s, int T, int bn_max, int* chunk_count, int* expert_offset,
-                                 int4* tiles, int* tile_done, cudaStream_t st);
-cudaError_t launch_dispatch_scatter(const Shape& s, const int32_t* topk_idx, int T, const int* chunk_base,
-                                    int* perm_src, int* inv_slot, int* status, cudaStream_t st);
-cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, int rows, bf16* x_perm,
-                               int* status, int num_sms, cudaStream_t st);
+// Dispatch of the (token, slot) pairs routed to experts [e_lo, e_lo + E_loc) (all experts,
+// or one expert-parallel shard; other pairs get inv_slot = -1). Work-list expert ids are
+// local (e - e_lo).
+cudaError_t launch_dispatch_count(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T, int* chunk_count,
+                                  int* status, cudaStream_t st);
+cudaError_t launch_dispatch_scan(int E_loc, int T, int bn_max, int* chunk_count, int* expert_offset, int4* tiles,
+                                 int* tile_done, cudaStream_t st);
+cudaError_t launch_dispatch_scatter(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T,
+                                    const int* chunk_base, int* perm_src, int* inv_slot, int* status, cudaStream_t st);
+// x_perm[row] = x[perm_src[row]] for the *n_rows rows dispatched (rows: an upper bound).
+cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, const int* n_rows, int rows,
+                               bf16* x_perm, int* status, int num_sms, cudaStream_t st);
 
 // ---------------------------------------------------------------- expert MLP (expert_mlp.cu)
 // Largest N-tile (token rows per tile) the expert kernel uses for a batch of T tokens.
@@ -72,6 +76,9 @@ cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int 
 // ---------------------------------------------------------------- combine (combine.cu)
 cudaError_t launch_combine(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T, bf16* out,
                            int* status, cudaStream_t st);
+// Shard combine: FP32 partial sums over the slots of this shard (inv_slot >= 0).
+cudaError_t launch_combine_partial(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T,
+                                   float* out, int* status, cudaStream_t st);
 
 // ---------------------------------------------------------------- C-ABI helpers (api.cu)
 // The calling thread's error message (what beam_moe_last_error returns) and the argument

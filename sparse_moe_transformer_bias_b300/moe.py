@@ -4,6 +4,7 @@
     idx, w = moe.route(x, router_w, bias, shape=workloads.TINY)
     logits = moe.router_logits(x, router_w)
     out = moe.forward_host(x_pinned, ...)     # host in, host out (copies on the stream)
+    part = moe.forward_shard(x, router_w, bias, wg[lo:hi], wu[lo:hi], wd[lo:hi], lo, hi)  # FP32
     x = moe.rmsnorm(stream, gamma, eps)
     new_stream = moe.sublayer_forward(stream, pre_gamma, post_gamma, eps, k, router_w, bias, w_gate, w_up, w_down)
 
@@ -96,4 +97,19 @@ def sublayer_forward(stream_in, pre_gamma, post_gamma, eps: float, k: int, route
         out = torch.empty_like(stream_in)
     abi.beam_moe_sublayer_forward(shape, stream_in, pre_gamma, post_gamma, eps, k, router_w, bias, w_gate, w_up,
                                   w_down, T, out, stream)
+    return out
+
+
+def forward_shard(x, router_w, bias, w_gate, w_up, w_down, e_begin: int, e_end: int, shape: MoEShape = BEAM,
+                  out=None, stream=None):
+    """One expert-parallel shard: this device's experts [e_begin, e_end) (w_* hold only
+    those); returns the FP32 partial output over the slots routed to them. Summing the
+    partials of shards covering every expert gives the block's output."""
+    T = _check_inputs(shape, x, router_w, bias)
+    n = e_end - e_begin
+    for w, rows, cols in ((w_gate, shape.I, shape.d), (w_up, shape.I, shape.d), (w_down, shape.d, shape.I)):
+        assert w.dtype == torch.bfloat16 and w.shape == (n, rows, cols) and w.is_contiguous()
+    if out is None:
+        out = torch.empty((T, shape.d), dtype=torch.float32, device=x.device)
+    abi.beam_moe_forward_shard(shape, x, router_w, bias, w_gate, w_up, w_down, e_begin, e_end, T, out, stream)
     return out

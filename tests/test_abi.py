@@ -92,3 +92,13 @@ def test_binding_raises_with_message(lib):
 
 def test_tiny_shape_accepted_by_checks(lib):
     assert call_forward(abi.BeamMoeConfig.of(W.TINY), T=0) == abi.BEAM_MOE_OK
+
+
+def test_shard_range_rejected(lib):
+    cfg = cfg_of()
+    for lo, hi in ((0, 0), (5, 3), (-1, 4), (0, 257)):
+        rc = lib.beam_moe_forward_shard(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, lo, hi, 4, FAKE, None)
+        assert rc == abi.BEAM_MOE_ERR_ARG, (lo, hi)
+        assert "expert range" in abi.beam_moe_last_error()
+    assert lib.beam_moe_forward_shard(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 32, 0, FAKE,
+                                      None) == abi.BEAM_MOE_OK
