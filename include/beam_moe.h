@@ -126,6 +126,18 @@ BEAM_MOE_API int beam_moe_forward_shard(const beam_moe_config *cfg, const __nv_b
                            const __nv_bfloat16 *w_down, int e_begin, int e_end, int T, float *out_partial,
                            cudaStream_t stream);
 
+/* Dense SwiGLU MLP of the first decoder layers (Glonce "Reflection releases Beam ...",
+ * Architecture paragraph: the first 3 layers are dense SwiGLU MLPs; transformers "Beam" doc:
+ * mlp_layer_types sets the pattern, SwiGLU activation in FP32). The pages give no width for
+ * it, so I is the caller's:
+ *   out[t] = w_down . ( silu(w_gate . x[t]) * (w_up . x[t]) ),  silu(z) = z sigmoid(z)
+ *   x, out bf16 [T, d]; w_gate, w_up bf16 [I, d]; w_down bf16 [d, I]; d, I multiples of 128.
+ * Same kernel and numerics as the experts (BF16 products, FP32 accumulation and activation,
+ * the activation rounded to BF16 for the down product), output rounded once to BF16. */
+BEAM_MOE_API int beam_moe_dense_mlp(int d, int I, const __nv_bfloat16 *x, const __nv_bfloat16 *w_gate,
+                       const __nv_bfloat16 *w_up, const __nv_bfloat16 *w_down, int T, __nv_bfloat16 *out,
+                       cudaStream_t stream);
+
 /* Pre-norm of the MoE sublayer (transformers "Beam" doc, Overview, "Sandwich norms with
  * depth-scaled residuals" bullet: each block is wrapped in an RMSNorm before and after;
  * the paragraph after the bullets: RMSNorm scaling is computed in FP32):

@@ -305,7 +305,7 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
             LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
                                                dev->status, dev->num_sms, st));
             LAUNCH(kExpert, launch_expert_mlp(se, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
-                                              bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
+                                              bn_max, sc.h, sc.y, nullptr, dev->status, dev->num_sms, st));
             if (mode == 4)
                 LAUNCH(kCombine, launch_combine_partial(s, sc.y, sc.inv_slot, w, T, shard->out_partial, dev->status,
                                                         st));
@@ -397,6 +397,47 @@ int beam_moe_forward_shard(const beam_moe_config* cfg, const __nv_bfloat16* x, c
     const ShardArgs sh{e_begin, e_end, out_partial};
     return run(cfg, x, router_w, expert_bias, w_gate, w_up, w_down, T, nullptr, nullptr, nullptr, nullptr, 4, stream,
                nullptr, &sh);
+}
+
+int beam_moe_dense_mlp(int d, int I, const __nv_bfloat16* x, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
+                       const __nv_bfloat16* w_down, int T, __nv_bfloat16* out, cudaStream_t stream) {
+    g_launches = 0;
+    timing_begin_call();
+    int rc;
+    if (d < 128 || d % 128) return fail(BEAM_MOE_ERR_ARG, "d=%d must be a positive multiple of 128", d);
+    if (I < 128 || I % 128) return fail(BEAM_MOE_ERR_ARG, "I=%d must be a positive multiple of 128", I);
+    if ((rc = check_T(T)) || (rc = check_ptr(x, "x")) || (rc = check_ptr(w_gate, "w_gate")) ||
+        (rc = check_ptr(w_up, "w_up")) || (rc = check_ptr(w_down, "w_down")) || (rc = check_ptr(out, "out")))
+        return rc;
+    if (T == 0) return BEAM_MOE_OK;
+    if ((rc = check_stream(stream))) return rc;
+    DeviceState* dev = nullptr;
+    if ((rc = device_state(&dev))) return rc;
+    const Shape s{d, I, 1, 1, 1, 1, 1.0f};
+    const int bn_max = gemm_bn_max(s, T);
+    const int max_tiles = dense_max_tiles(T, bn_max);
+    Carver c{nullptr};
+    c.take<int4>(1 + static_cast<size_t>(max_tiles));
+    c.take<int>(static_cast<size_t>(max_tiles));
+    c.take<bf16>(static_cast<size_t>(T) * I);
+    const size_t bytes = c.off + 256;
+    void* mem = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, stream);
+    if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "scratch allocation of %zu bytes: %s", bytes, cudaGetErrorString(e));
+    Carver cc{static_cast<char*>(mem)};
+    int4* tiles = cc.take<int4>(1 + static_cast<size_t>(max_tiles));
+    int* tile_done = cc.take<int>(static_cast<size_t>(max_tiles));
+    bf16* h = cc.take<bf16>(static_cast<size_t>(T) * I);
+    const cudaStream_t st = stream;
+    rc = BEAM_MOE_OK;
+    LAUNCH(kCount, launch_dense_tiles(T, bn_max, tiles, tile_done, st));
+    LAUNCH(kExpert, launch_expert_mlp(s, w_gate, w_up, w_down, x, T, tiles, tile_done, max_tiles, bn_max, h, nullptr,
+                                      out, dev->status, dev->num_sms, st));
+done:
+    e = cudaFreeAsync(mem, stream);
+    if (rc == BEAM_MOE_OK && e != cudaSuccess)
+        rc = fail(BEAM_MOE_ERR_CUDA, "scratch release: %s", cudaGetErrorString(e));
+    return rc;
 }
 
 int beam_moe_rmsnorm(int d, const __nv_bfloat16* v, const __nv_bfloat16* gamma, float eps, int T,

@@ -14,6 +14,8 @@ template <bool kPartial>
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y, const int* __restrict__ inv_slot,
                                                       const float* __restrict__ topk_w, int K, int d4, int n_rows,
                                                       void* __restrict__ out, int* status) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     __shared__ int rows[32];
     __shared__ float ws[32];
@@ -65,8 +67,9 @@ cudaError_t launch_combine(const Shape& s, const float* y, const int* inv_slot, 
     int ysplit = 1;
     while (T * ysplit < 296 && ysplit * 256 * 2 <= d4) ysplit *= 2;
     const dim3 grid(T, ysplit);
-    combine_kernel<false><<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
+    const cudaError_t le_ = launch_pdl(combine_kernel<false>, dim3(grid), dim3(256), 0, st, reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
                                                 T * s.top_k, out, status);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
@@ -76,8 +79,9 @@ cudaError_t launch_combine_partial(const Shape& s, const float* y, const int* in
     int ysplit = 1;
     while (T * ysplit < 296 && ysplit * 256 * 2 <= d4) ysplit *= 2;
     const dim3 grid(T, ysplit);
-    combine_kernel<true><<<grid, 256, 0, st>>>(reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
+    const cudaError_t le_ = launch_pdl(combine_kernel<true>, dim3(grid), dim3(256), 0, st, reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
                                                T * s.top_k, out, status);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 

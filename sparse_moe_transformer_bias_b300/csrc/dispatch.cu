@@ -47,6 +47,8 @@ __device__ __forceinline__ void build_bitmap(uint32_t* bm, const int32_t* __rest
 __global__ void __launch_bounds__(kChunk) dispatch_count_kernel(const int32_t* __restrict__ idx, int T, int E_all,
                                                                 int e_lo, int E, int K,
                                                                 int* __restrict__ chunk_count, int* status) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ uint32_t bm[];
     build_bitmap(bm, idx, T, E_all, e_lo, E, K, blockIdx.x * kChunk, status);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -63,6 +65,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int nchunks, int E,
                                                              int* __restrict__ expert_offset,
                                                              int4* __restrict__ tiles,
                                                              int* __restrict__ tile_done) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int tot[1024];
     __shared__ int ntl[1024];
     const int e = threadIdx.x;
@@ -118,6 +122,8 @@ __global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(const int32_t*
                                                                   const int* __restrict__ chunk_base,
                                                                   int* __restrict__ perm_src,
                                                                   int* __restrict__ inv_slot, int* status) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ uint32_t bm[];
     const int t0 = blockIdx.x * kChunk;
     build_bitmap(bm, idx, T, E_all, e_lo, E, K, t0, status);
@@ -148,6 +154,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int* __restrict__ perm_src,
                                                           const int* __restrict__ n_rows,
                                                           uint4* __restrict__ x_perm, int* status) {
+    pdl_wait();
+    pdl_trigger();
     const size_t total = static_cast<size_t>(*n_rows) * row_vecs;  // rows this call dispatched
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -174,14 +182,16 @@ cudaError_t launch_dispatch_count(const Shape& s, int e_lo, int E_loc, const int
                                   int* status, cudaStream_t st) {
     const int nchunks = (T + kChunk - 1) / kChunk;
     const size_t smem = static_cast<size_t>(E_loc) * kWords * sizeof(uint32_t);
-    dispatch_count_kernel<<<nchunks, kChunk, smem, st>>>(topk_idx, T, s.E, e_lo, E_loc, s.top_k, chunk_count, status);
+    const cudaError_t le_ = launch_pdl(dispatch_count_kernel, dim3(nchunks), dim3(kChunk), smem, st, topk_idx, T, s.E, e_lo, E_loc, s.top_k, chunk_count, status);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_scan(int E_loc, int T, int bn_max, int* chunk_count, int* expert_offset, int4* tiles,
                                  int* tile_done, cudaStream_t st) {
     const int nchunks = (T + kChunk - 1) / kChunk;
-    dispatch_scan_kernel<<<1, 1024, 0, st>>>(nchunks, E_loc, bn_max, chunk_count, expert_offset, tiles, tile_done);
+    const cudaError_t le_ = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, nchunks, E_loc, bn_max, chunk_count, expert_offset, tiles, tile_done);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
@@ -189,8 +199,9 @@ cudaError_t launch_dispatch_scatter(const Shape& s, int e_lo, int E_loc, const i
                                     const int* chunk_base, int* perm_src, int* inv_slot, int* status, cudaStream_t st) {
     const int nchunks = (T + kChunk - 1) / kChunk;
     const size_t smem = static_cast<size_t>(E_loc) * kWords * sizeof(uint32_t);
-    dispatch_scatter_kernel<<<nchunks, kChunk, smem, st>>>(topk_idx, T, s.E, e_lo, E_loc, s.top_k, chunk_base, perm_src,
+    const cudaError_t le_ = launch_pdl(dispatch_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, st, topk_idx, T, s.E, e_lo, E_loc, s.top_k, chunk_base, perm_src,
                                                            inv_slot, status);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
@@ -202,9 +213,10 @@ cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src,
     const long long cap = static_cast<long long>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const uint4*>(x), row_vecs, T,
+    const cudaError_t le_ = launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, reinterpret_cast<const uint4*>(x), row_vecs, T,
                                                                       perm_src, n_rows,
                                                                       reinterpret_cast<uint4*>(x_perm), status);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 

@@ -85,6 +85,7 @@ struct MlpArgs {
     int I, d;
     bf16* h;
     float* y;
+    bf16* y_bf16;        // if set, down items store BF16 here instead of FP32 y (dense MLP)
     int* status;
 };
 
@@ -187,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // the prologue above touches no global memory
+    pdl_trigger();
     int n_tiles = args.tiles[0].x;
     if (n_tiles < 0 || n_tiles > args.max_tiles) {
         if (threadIdx.x == 0) flag_status(status, kStatusBadIndex);
@@ -390,7 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (c0 + j < it.tl.z) {
                             const float gv = __uint_as_float(g[j]);
                             const float uv = __uint_as_float(u[j]);
-                            const float hv = gv / (1.0f + expf(-gv)) * uv;
+                            // silu(g) * u in FP32 with the fast exponential and division
+                            // (a few ulp; the result is rounded to BF16 next)
+                            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                             args.h[static_cast<size_t>(it.tl.y + c0 + j) * args.I + col] = __float2bfloat16_rn(hv);
                         }
                     }
@@ -401,9 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < it.tl.z) {
-                            float* yr = args.y + static_cast<size_t>(it.tl.y + c0 + j) * args.d;
-                            yr[col] = __uint_as_float(g[j]);
-                            if (col1_ok) yr[col + kTileM] = __uint_as_float(g1[j]);
+                            const size_t r0 = static_cast<size_t>(it.tl.y + c0 + j) * args.d;
+                            if (args.y_bf16) {
+                                args.y_bf16[r0 + col] = __float2bfloat16_rn(__uint_as_float(g[j]));
+                                if (col1_ok) args.y_bf16[r0 + col + kTileM] = __float2bfloat16_rn(__uint_as_float(g1[j]));
+                            } else {
+                                args.y[r0 + col] = __uint_as_float(g[j]);
+                                if (col1_ok) args.y[r0 + col + kTileM] = __uint_as_float(g1[j]);
+                            }
                         }
                     }
                 }
@@ -443,7 +453,8 @@ cudaError_t launch_mlp(const CUtensorMap& wg, const CUtensorMap& wu, const CUten
     auto kern = expert_mlp_kernel<kBNMax>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, C::kSmemBytes, st>>>(wg, wu, wd, x, h, args);
+    const cudaError_t le_ = launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, st, wg, wu, wd, x, h, args);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
@@ -459,9 +470,38 @@ int gemm_bn_max(const Shape& s, int T) {
     return avg_rows <= 32 ? 128 : 256;
 }
 
+namespace {
+
+// Work list of one "expert" holding every token in order (the dense MLP): N-tiles of at
+// most bn_max rows, split evenly like dispatch does; counters zeroed.
+__global__ void __launch_bounds__(256) dense_tiles_kernel(int T, int bn_max, int4* __restrict__ tiles,
+                                                          int* __restrict__ tile_done) {
+    pdl_wait();
+    pdl_trigger();
+    const int q = (T + bn_max - 1) / bn_max;
+    const int per = min(bn_max, (((T + q - 1) / q + 15) / 16) * 16);
+    const int nt = (T + per - 1) / per;
+    for (int i = threadIdx.x; i < nt; i += blockDim.x) {
+        tiles[1 + i] = make_int4(0, i * per, min(per, T - i * per), 0);
+        tile_done[i] = 0;
+    }
+    if (threadIdx.x == 0) tiles[0] = make_int4(nt, 0, 0, 0);
+}
+
+}  // namespace
+
+int dense_max_tiles(int T, int bn_max) { return T / bn_max + 2; }
+
+cudaError_t launch_dense_tiles(int T, int bn_max, int4* tiles, int* tile_done, cudaStream_t st) {
+    const cudaError_t le_ = launch_pdl(dense_tiles_kernel, dim3(1), dim3(256), 0, st, T, bn_max, tiles, tile_done);
+    if (le_ != cudaSuccess) return le_;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* w_down,
                               const bf16* x_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
-                              int bn_max, bf16* h, float* y, int* status, int num_sms, cudaStream_t st) {
+                              int bn_max, bf16* h, float* y, bf16* y_bf16, int* status, int num_sms,
+                              cudaStream_t st) {
     CUtensorMap wg, wu, wd;
     BMaps bx, bh;
     const char* why = nullptr;
@@ -485,6 +525,7 @@ cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_
     a.d = s.d;
     a.h = h;
     a.y = y;
+    a.y_bf16 = y_bf16;
     a.status = status;
     const long long items = static_cast<long long>(max_tiles) * (a.m_gu + a.m_dn);
     const int grid = static_cast<int>(items < num_sms ? (items < 1 ? 1 : items) : num_sms);

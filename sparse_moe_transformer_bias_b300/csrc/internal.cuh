@@ -11,6 +11,34 @@ namespace beam {
 
 using bf16 = __nv_bfloat16;
 
+// Programmatic dependent launch. Every kernel of the library is launched with
+// launch_pdl, so it may start while its predecessor in the stream finishes; each kernel
+// calls pdl_wait() before its first global-memory access (read or write), which returns
+// once every earlier kernel has completed and its memory is visible, so memory effects
+// keep stream order (scratch reuse through the stream-ordered pool included).
+// pdl_trigger() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+#ifdef BEAM_NO_PDL
+    cfg.numAttrs = 0;
+#else
+    cfg.numAttrs = 1;
+#endif
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 struct Shape {
     int d, I, E, n_group, topk_group, top_k;
     float scale;
@@ -64,7 +92,11 @@ int gemm_bn_max(const Shape& s, int T);
 // and the work list's item counter must be zero (dispatch_scan sets them).
 cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* w_down,
                               const bf16* x_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
-                              int bn_max, bf16* h, float* y, int* status, int num_sms, cudaStream_t st);
+                              int bn_max, bf16* h, float* y, bf16* y_bf16, int* status, int num_sms,
+                              cudaStream_t st);
+// Dense MLP (one "expert", every token in order): the work list and its capacity.
+int dense_max_tiles(int T, int bn_max);
+cudaError_t launch_dense_tiles(int T, int bn_max, int4* tiles, int* tile_done, cudaStream_t st);
 
 // ---------------------------------------------------------------- router product (router_gemm.cu)
 // Split-K count of the tensor-core router product for T tokens.

@@ -53,6 +53,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint2* __restrict__ v,
                                                                const uint2* __restrict__ gamma, float eps, int d4,
                                                                uint2* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[kNormThreads / 32];
     const size_t row = static_cast<size_t>(blockIdx.x) * d4;
     float4 x[kNormMaxVec];
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(kNormThreads) combine_residual_kernel(
     const float4* __restrict__ y, const int* __restrict__ inv_slot, const float* __restrict__ topk_w, int K, int d4,
     int n_rows, const uint2* stream_in, const uint2* __restrict__ gamma, float eps, float a, float b,
     uint2* stream_out, int* status) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int rows[32];
     __shared__ float ws[32];
     __shared__ float red[kNormThreads / 32];
@@ -142,8 +146,9 @@ __global__ void __launch_bounds__(kNormThreads) combine_residual_kernel(
 
 cudaError_t launch_rmsnorm(int d, const bf16* v, const bf16* gamma, float eps, int T, bf16* out, cudaStream_t st) {
     if (d % 4 || d > kNormMaxD) return cudaErrorInvalidValue;
-    rmsnorm_kernel<<<T, kNormThreads, 0, st>>>(reinterpret_cast<const uint2*>(v), reinterpret_cast<const uint2*>(gamma),
+    const cudaError_t le_ = launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, reinterpret_cast<const uint2*>(v), reinterpret_cast<const uint2*>(gamma),
                                                eps, d / 4, reinterpret_cast<uint2*>(out));
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
@@ -153,10 +158,11 @@ cudaError_t launch_combine_residual(const Shape& s, const float* y, const int* i
     if (s.d % 4 || s.d > kNormMaxD || k_contrib < 2) return cudaErrorInvalidValue;
     const float a = static_cast<float>(sqrt(static_cast<double>(k_contrib - 1) / k_contrib));
     const float b = static_cast<float>(1.0 / sqrt(static_cast<double>(k_contrib)));
-    combine_residual_kernel<<<T, kNormThreads, 0, st>>>(
+    const cudaError_t le_ = launch_pdl(combine_residual_kernel, dim3(T), dim3(kNormThreads), 0, st, 
         reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, s.d / 4, T * s.top_k,
         reinterpret_cast<const uint2*>(stream_in), reinterpret_cast<const uint2*>(gamma), eps, a, b,
         reinterpret_cast<uint2*>(stream_out), status);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 

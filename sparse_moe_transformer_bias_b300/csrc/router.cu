@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32) router_logits_small_kernel(c
                                                                               const float* __restrict__ wr, int T,
                                                                               int d, int E,
                                                                               float* __restrict__ logits) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[kSmallWarps][kSmallT * kSmallEPB];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * kSmallEPB;
@@ -107,6 +109,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
                                                             int32_t* __restrict__ topk_idx,
                                                             float* __restrict__ topk_w,
                                                             float* __restrict__ logits_out) {
+    pdl_wait();
+    pdl_trigger();
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -208,6 +212,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
 // plus 16 binades, far below any router weight).
 __global__ void __launch_bounds__(256) router_split_weights_kernel(const float4* __restrict__ w, size_t n4,
                                                                   size_t n, bf16* __restrict__ w3) {
+    pdl_wait();
+    pdl_trigger();
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const float4 v = w[i];
@@ -249,8 +255,9 @@ cudaError_t launch_router_split_weights(const Shape& s, const float* wr, bf16* w
     long long blocks = static_cast<long long>((n4 + 255) / 256);
     const long long cap = static_cast<long long>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    router_split_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const float4*>(wr),
+    const cudaError_t le_ = launch_pdl(router_split_weights_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, reinterpret_cast<const float4*>(wr),
                                                                                n4, n, w3);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
@@ -258,8 +265,9 @@ cudaError_t launch_router_logits(const Shape& s, const RouterPlan& p, const bf16
                                  const bf16* w3, float* partial, int* status, int num_sms, cudaStream_t st) {
     if (!p.tensor) {
         if (p.splits != 1 || T > kSmallT) return cudaErrorInvalidValue;
-        router_logits_small_kernel<<<(s.E + kSmallEPB - 1) / kSmallEPB, kSmallWarps * 32, 0, st>>>(x, wr, T, s.d, s.E,
+        const cudaError_t le_ = launch_pdl(router_logits_small_kernel, dim3((s.E + kSmallEPB - 1) / kSmallEPB), dim3(kSmallWarps * 32), 0, st, x, wr, T, s.d, s.E,
                                                                                                 partial);
+    if (le_ != cudaSuccess) return le_;
         return cudaGetLastError();
     }
     return launch_router_tc(s, w3, x, T, p.splits, partial, status, num_sms, st);
@@ -269,9 +277,10 @@ cudaError_t launch_router_select(const Shape& s, const float* partial, int split
                                  int32_t* topk_idx, float* topk_w, float* logits_out, cudaStream_t st) {
     const int warps_per_block = 8;
     const int blocks = (T + warps_per_block - 1) / warps_per_block;
-    router_select_kernel<<<blocks, warps_per_block * 32, 0, st>>>(partial, splits, bias, T, s.E, s.n_group,
+    const cudaError_t le_ = launch_pdl(router_select_kernel, dim3(blocks), dim3(warps_per_block * 32), 0, st, partial, splits, bias, T, s.E, s.n_group,
                                                                   s.topk_group, s.top_k, s.scale, topk_idx, topk_w,
                                                                   logits_out);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 

@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // the prologue above touches no global memory
+    pdl_trigger();
     const int n_items = ((args.T + kBN - 1) / kBN) * args.m_tiles * args.splits;
     const int k_chunks = args.k_chunks;
 
@@ -314,7 +316,8 @@ cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int 
     cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    router_gemm_kernel<<<grid, kThreads, Cfg::kSmemBytes, st>>>(w, b, a);
+    const cudaError_t le_ = launch_pdl(router_gemm_kernel, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, st, w, b, a);
+    if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 

@@ -113,3 +113,16 @@ def forward_shard(x, router_w, bias, w_gate, w_up, w_down, e_begin: int, e_end: 
         out = torch.empty((T, shape.d), dtype=torch.float32, device=x.device)
     abi.beam_moe_forward_shard(shape, x, router_w, bias, w_gate, w_up, w_down, e_begin, e_end, T, out, stream)
     return out
+
+
+def dense_mlp(x, w_gate, w_up, w_down, out=None, stream=None):
+    """Dense SwiGLU MLP on BF16 [T, d] tokens with weights [I, d], [I, d], [d, I]."""
+    T, d = x.shape
+    I = w_gate.shape[0]
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
+    for w, shp in ((w_gate, (I, d)), (w_up, (I, d)), (w_down, (d, I))):
+        assert w.dtype == torch.bfloat16 and tuple(w.shape) == shp and w.is_contiguous()
+    if out is None:
+        out = torch.empty_like(x)
+    abi.beam_moe_dense_mlp(d, I, x, w_gate, w_up, w_down, T, out, stream)
+    return out

@@ -102,3 +102,12 @@ def test_shard_range_rejected(lib):
         assert "expert range" in abi.beam_moe_last_error()
     assert lib.beam_moe_forward_shard(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 32, 0, FAKE,
                                       None) == abi.BEAM_MOE_OK
+
+
+def test_dense_mlp_arguments_checked(lib):
+    f = lib.beam_moe_dense_mlp
+    assert f(100, 256, FAKE, FAKE, FAKE, FAKE, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert f(512, 200, FAKE, FAKE, FAKE, FAKE, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert f(512, 256, FAKE, None, FAKE, FAKE, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert f(512, 256, FAKE, FAKE, FAKE, FAKE + 8, 4, FAKE, None) == abi.BEAM_MOE_ERR_ALIGN
+    assert f(512, 256, FAKE, FAKE, FAKE, FAKE, 0, FAKE, None) == abi.BEAM_MOE_OK
