@@ -139,9 +139,9 @@ def algorithmic(shape, T, n_touched, rows):
     d, I, E, K = shape.d, shape.I, shape.E, shape.top_k
     layer_flops = T * (K * 3 * 2 * d * I + 2 * d * E)
     layer_bytes = n_touched * 3 * d * I * 2 + E * d * 4 + E * 4 + 2 * T * d * 2 + T * K * 8
-    # weights once; x_perm read, h written and read back, y written
+    # weights once; x_perm read, h written and read back, y (BF16) written
     mlp = {"flops": 2 * rows * d * I * 3,
-           "bytes": n_touched * 3 * I * d * 2 + rows * d * 2 + 2 * rows * I * 2 + rows * d * 4}
+           "bytes": n_touched * 3 * I * d * 2 + rows * d * 2 + 2 * rows * I * 2 + rows * d * 2}
     return layer_flops, layer_bytes, {"expert_mlp": mlp}
 
 

@@ -145,7 +145,7 @@ struct Scratch {
     int* inv_slot = nullptr;
     bf16* x_perm = nullptr;
     bf16* h = nullptr;
-    float* y = nullptr;
+    bf16* y = nullptr;
 };
 
 struct Carver {
@@ -182,7 +182,7 @@ size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool
         sc->inv_slot = c.take<int>(pairs);
         sc->x_perm = c.take<bf16>(pairs * s.d);
         sc->h = c.take<bf16>(pairs * s.I);
-        sc->y = c.take<float>(pairs * s.d);
+        sc->y = c.take<bf16>(pairs * s.d);
     }
     return c.off + 256;
 }
@@ -305,7 +305,7 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
             LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
                                                dev->status, dev->num_sms, st));
             LAUNCH(kExpert, launch_expert_mlp(se, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
-                                              bn_max, sc.h, sc.y, nullptr, dev->status, dev->num_sms, st));
+                                              bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
             if (mode == 4)
                 LAUNCH(kCombine, launch_combine_partial(s, sc.y, sc.inv_slot, w, T, shard->out_partial, dev->status,
                                                         st));
@@ -431,8 +431,8 @@ int beam_moe_dense_mlp(int d, int I, const __nv_bfloat16* x, const __nv_bfloat16
     const cudaStream_t st = stream;
     rc = BEAM_MOE_OK;
     LAUNCH(kCount, launch_dense_tiles(T, bn_max, tiles, tile_done, st));
-    LAUNCH(kExpert, launch_expert_mlp(s, w_gate, w_up, w_down, x, T, tiles, tile_done, max_tiles, bn_max, h, nullptr,
-                                      out, dev->status, dev->num_sms, st));
+    LAUNCH(kExpert, launch_expert_mlp(s, w_gate, w_up, w_down, x, T, tiles, tile_done, max_tiles, bn_max, h, out,
+                                      dev->status, dev->num_sms, st));
 done:
     e = cudaFreeAsync(mem, stream);
     if (rc == BEAM_MOE_OK && e != cudaSuccess)

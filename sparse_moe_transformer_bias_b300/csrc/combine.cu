@@ -2,7 +2,8 @@
 // outputs are combined with normalized router weights, scaled by 2.5 - the scale is
 // already inside the weights): out[t] = sum_k w[t,k] * y[inv_slot[t,k]], FP32 fused
 // multiply-adds in slot order k = 0..top_k-1 (a gather, so the order is fixed and the
-// result deterministic), rounded once to BF16. 16-byte loads of y, 8-byte stores of out.
+// result deterministic), rounded once to BF16. y (the experts' BF16 outputs) is read in
+// 8-byte loads of four values, out stored in 8-byte stores.
 // Shard mode (expert parallelism): slots routed to another shard (inv_slot = -1) are left
 // out and the FP32 partial sum is stored unrounded, for the sum over shards.
 #include "internal.cuh"
@@ -11,7 +12,7 @@ namespace beam {
 namespace {
 
 template <bool kPartial>
-__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y, const int* __restrict__ inv_slot,
+__global__ void __launch_bounds__(256) combine_kernel(const uint2* __restrict__ y, const int* __restrict__ inv_slot,
                                                       const float* __restrict__ topk_w, int K, int d4, int n_rows,
                                                       void* __restrict__ out, int* status) {
     pdl_wait();
@@ -39,7 +40,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
         for (int k = 0; k < K; ++k) {
             const float w = ws[k];
             if (kPartial && w == 0.f) continue;
-            const float4 v = y[static_cast<size_t>(rows[k]) * d4 + c];
+            const uint2 raw = y[static_cast<size_t>(rows[k]) * d4 + c];
+            const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+            const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+            const float4 v = make_float4(v01.x, v01.y, v23.x, v23.y);
             acc.x = fmaf(w, v.x, acc.x);
             acc.y = fmaf(w, v.y, acc.y);
             acc.z = fmaf(w, v.z, acc.z);
@@ -60,26 +64,26 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
 
 }  // namespace
 
-cudaError_t launch_combine(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T, bf16* out,
+cudaError_t launch_combine(const Shape& s, const bf16* y, const int* inv_slot, const float* topk_w, int T, bf16* out,
                            int* status, cudaStream_t st) {
     const int d4 = s.d / 4;
     // Split the row across a few blocks when there are few tokens.
     int ysplit = 1;
     while (T * ysplit < 296 && ysplit * 256 * 2 <= d4) ysplit *= 2;
     const dim3 grid(T, ysplit);
-    const cudaError_t le_ = launch_pdl(combine_kernel<false>, dim3(grid), dim3(256), 0, st, reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
+    const cudaError_t le_ = launch_pdl(combine_kernel<false>, dim3(grid), dim3(256), 0, st, reinterpret_cast<const uint2*>(y), inv_slot, topk_w, s.top_k, d4,
                                                 T * s.top_k, out, status);
     if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine_partial(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T,
+cudaError_t launch_combine_partial(const Shape& s, const bf16* y, const int* inv_slot, const float* topk_w, int T,
                                    float* out, int* status, cudaStream_t st) {
     const int d4 = s.d / 4;
     int ysplit = 1;
     while (T * ysplit < 296 && ysplit * 256 * 2 <= d4) ysplit *= 2;
     const dim3 grid(T, ysplit);
-    const cudaError_t le_ = launch_pdl(combine_kernel<true>, dim3(grid), dim3(256), 0, st, reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, d4,
+    const cudaError_t le_ = launch_pdl(combine_kernel<true>, dim3(grid), dim3(256), 0, st, reinterpret_cast<const uint2*>(y), inv_slot, topk_w, s.top_k, d4,
                                                T * s.top_k, out, status);
     if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();

@@ -10,7 +10,8 @@
 //   gate/up item (tile, m), m < I/128: two accumulators (gate, up) share the token rows;
 //          the epilogue computes silu(g) * u in FP32 and stores BF16 h;
 //   down item (tile, p), p < d/256: two accumulators for the weight tiles 2p and 2p+1
-//          (two adjacent 128-row tiles of Wd) sharing the h rows; the epilogue stores FP32 y.
+//          (two adjacent 128-row tiles of Wd) sharing the h rows; the epilogue rounds the
+//          FP32 accumulators to BF16 y (the expert output, in the model's dtype).
 // So every item streams two 128-row weight tiles against one set of token rows per K
 // step and fills the same stage layout.
 // Item ids run over every gate/up item, then every down item; CTAs take the next id from
@@ -84,8 +85,7 @@ struct MlpArgs {
     int kc_gu, kc_dn;    // K chunks: d / 64, I / 64
     int I, d;
     bf16* h;
-    float* y;
-    bf16* y_bf16;        // if set, down items store BF16 here instead of FP32 y (dense MLP)
+    bf16* y;             // [rows, d] expert outputs (the dense MLP: its output)
     int* status;
 };
 
@@ -407,13 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < it.tl.z) {
                             const size_t r0 = static_cast<size_t>(it.tl.y + c0 + j) * args.d;
-                            if (args.y_bf16) {
-                                args.y_bf16[r0 + col] = __float2bfloat16_rn(__uint_as_float(g[j]));
-                                if (col1_ok) args.y_bf16[r0 + col + kTileM] = __float2bfloat16_rn(__uint_as_float(g1[j]));
-                            } else {
-                                args.y[r0 + col] = __uint_as_float(g[j]);
-                                if (col1_ok) args.y[r0 + col + kTileM] = __uint_as_float(g1[j]);
-                            }
+                            args.y[r0 + col] = __float2bfloat16_rn(__uint_as_float(g[j]));
+                            if (col1_ok) args.y[r0 + col + kTileM] = __float2bfloat16_rn(__uint_as_float(g1[j]));
                         }
                     }
                 }
@@ -500,7 +495,7 @@ cudaError_t launch_dense_tiles(int T, int bn_max, int4* tiles, int* tile_done, c
 
 cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* w_down,
                               const bf16* x_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
-                              int bn_max, bf16* h, float* y, bf16* y_bf16, int* status, int num_sms,
+                              int bn_max, bf16* h, bf16* y, int* status, int num_sms,
                               cudaStream_t st) {
     CUtensorMap wg, wu, wd;
     BMaps bx, bh;
@@ -525,7 +520,6 @@ cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_
     a.d = s.d;
     a.h = h;
     a.y = y;
-    a.y_bf16 = y_bf16;
     a.status = status;
     const long long items = static_cast<long long>(max_tiles) * (a.m_gu + a.m_dn);
     const int grid = static_cast<int>(items < num_sms ? (items < 1 ? 1 : items) : num_sms);

@@ -88,11 +88,11 @@ cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src,
 // Largest N-tile (token rows per tile) the expert kernel uses for a batch of T tokens.
 int gemm_bn_max(const Shape& s, int T);
 // Both expert products in one persistent kernel (expert_mlp.cu): h = SwiGLU(x_perm) and
-// y = h . Wd^T per N-tile of the work list, scheduled dynamically; tile_done[max_tiles]
+// y = h . Wd^T (BF16) per N-tile of the work list, scheduled dynamically; tile_done[max_tiles]
 // and the work list's item counter must be zero (dispatch_scan sets them).
 cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* w_down,
                               const bf16* x_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
-                              int bn_max, bf16* h, float* y, bf16* y_bf16, int* status, int num_sms,
+                              int bn_max, bf16* h, bf16* y, int* status, int num_sms,
                               cudaStream_t st);
 // Dense MLP (one "expert", every token in order): the work list and its capacity.
 int dense_max_tiles(int T, int bn_max);
@@ -106,10 +106,10 @@ cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int 
                              int* status, int num_sms, cudaStream_t st);
 
 // ---------------------------------------------------------------- combine (combine.cu)
-cudaError_t launch_combine(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T, bf16* out,
+cudaError_t launch_combine(const Shape& s, const bf16* y, const int* inv_slot, const float* topk_w, int T, bf16* out,
                            int* status, cudaStream_t st);
 // Shard combine: FP32 partial sums over the slots of this shard (inv_slot >= 0).
-cudaError_t launch_combine_partial(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T,
+cudaError_t launch_combine_partial(const Shape& s, const bf16* y, const int* inv_slot, const float* topk_w, int T,
                                    float* out, int* status, cudaStream_t st);
 
 // ---------------------------------------------------------------- C-ABI helpers (api.cu)
@@ -128,7 +128,7 @@ cudaError_t launch_rmsnorm(int d, const bf16* v, const bf16* gamma, float eps, i
 // Combine fused with the post-norm and the depth-scaled residual of contribution k:
 // stream_out[t] = sqrt((k-1)/k) stream_in[t] + gamma * m / sqrt(mean(m^2) + eps) / sqrt(k),
 // m = sum_k w[t,k] y[slot(t,k)] in FP32.
-cudaError_t launch_combine_residual(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T,
+cudaError_t launch_combine_residual(const Shape& s, const bf16* y, const int* inv_slot, const float* topk_w, int T,
                                     const bf16* stream_in, const bf16* gamma, float eps, int k_contrib,
                                     bf16* stream_out, int* status, cudaStream_t st);
 

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint2* __re
 }
 
 __global__ void __launch_bounds__(kNormThreads) combine_residual_kernel(
-    const float4* __restrict__ y, const int* __restrict__ inv_slot, const float* __restrict__ topk_w, int K, int d4,
+    const uint2* __restrict__ y, const int* __restrict__ inv_slot, const float* __restrict__ topk_w, int K, int d4,
     int n_rows, const uint2* stream_in, const uint2* __restrict__ gamma, float eps, float a, float b,
     uint2* stream_out, int* status) {
     pdl_wait();
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kNormThreads) combine_residual_kernel(
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c < d4) {
             for (int k = 0; k < K; ++k) {
-                const float4 v = y[static_cast<size_t>(rows[k]) * d4 + c];
+                const float4 v = bf16x4_to_float4(y[static_cast<size_t>(rows[k]) * d4 + c]);
                 const float w = ws[k];
                 acc.x = fmaf(w, v.x, acc.x);
                 acc.y = fmaf(w, v.y, acc.y);
@@ -152,14 +152,14 @@ cudaError_t launch_rmsnorm(int d, const bf16* v, const bf16* gamma, float eps, i
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine_residual(const Shape& s, const float* y, const int* inv_slot, const float* topk_w, int T,
+cudaError_t launch_combine_residual(const Shape& s, const bf16* y, const int* inv_slot, const float* topk_w, int T,
                                     const bf16* stream_in, const bf16* gamma, float eps, int k_contrib,
                                     bf16* stream_out, int* status, cudaStream_t st) {
     if (s.d % 4 || s.d > kNormMaxD || k_contrib < 2) return cudaErrorInvalidValue;
     const float a = static_cast<float>(sqrt(static_cast<double>(k_contrib - 1) / k_contrib));
     const float b = static_cast<float>(1.0 / sqrt(static_cast<double>(k_contrib)));
     const cudaError_t le_ = launch_pdl(combine_residual_kernel, dim3(T), dim3(kNormThreads), 0, st, 
-        reinterpret_cast<const float4*>(y), inv_slot, topk_w, s.top_k, s.d / 4, T * s.top_k,
+        reinterpret_cast<const uint2*>(y), inv_slot, topk_w, s.top_k, s.d / 4, T * s.top_k,
         reinterpret_cast<const uint2*>(stream_in), reinterpret_cast<const uint2*>(gamma), eps, a, b,
         reinterpret_cast<uint2*>(stream_out), status);
     if (le_ != cudaSuccess) return le_;
