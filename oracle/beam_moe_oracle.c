@@ -346,3 +346,57 @@ int oracle_round_bf16(int64_t n, const double *v, uint16_t *out)
     for (int64_t i = 0; i < n; i++) out[i] = bf16_round(v[i]);
     return ORACLE_OK;
 }
+
+/*
+ * FP8 E4M3 (the FP8 checkpoint format: [Glonce] Hardware paragraph, the FP8 checkpoint;
+ * [HF-doc] quantised checkpoints), decoded from the format's definition: bit 7 sign, bits
+ * 6-3 exponent with bias 7, bits 2-0 mantissa; exponent 0 is subnormal (m/8 * 2^-6); the
+ * codes 0x7F and 0xFF are NaN (returned as NaN); there are no infinities.
+ */
+static double e4m3_value(uint8_t q)
+{
+    const int sign = (q >> 7) & 1, e = (q >> 3) & 15, m = q & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+int oracle_e4m3_decode(int64_t n, const uint8_t *q, double *out)
+{
+    if (n < 0 || (n && (!q || !out))) return ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < n; i++) out[i] = e4m3_value(q[i]);
+    return ORACLE_OK;
+}
+
+/*
+ * One SwiGLU expert with FP8 weights, one FP32 scale per output row (weight-only
+ * quantisation; the pages give no recipe, this is the per-row reading): the weights are
+ * W[r][c] = scale[r] * e4m3(q[r][c]), and the expert is oracle_expert's, all in FP64:
+ *   g_i = sum_j x_j Wg[i][j],  u_i = sum_j x_j Wu[i][j],  h_i = g_i sigmoid(g_i) u_i,
+ *   y_j = sum_i h_i Wd[j][i]
+ * wg_q, wu_q [I][d] with gs, us [I]; wd_q [d][I] with ds [d].
+ */
+int oracle_expert_fp8(int d, int I, const double *x, const uint8_t *wg_q, const float *gs, const uint8_t *wu_q,
+                      const float *us, const uint8_t *wd_q, const float *ds, double *y)
+{
+    if (d <= 0 || I <= 0 || !x || !wg_q || !gs || !wu_q || !us || !wd_q || !ds || !y) return ORACLE_BAD_ARG;
+    double *h = (double *)malloc(sizeof(double) * I);
+    if (!h) return ORACLE_NO_MEM;
+    for (int i = 0; i < I; i++) {
+        double g = 0.0, u = 0.0;
+        for (int j = 0; j < d; j++) {
+            g += x[j] * ((double)gs[i] * e4m3_value(wg_q[(int64_t)i * d + j]));
+            u += x[j] * ((double)us[i] * e4m3_value(wu_q[(int64_t)i * d + j]));
+        }
+        h[i] = g * u / (1.0 + exp(-g));
+    }
+    for (int j = 0; j < d; j++) {
+        double acc = 0.0;
+        for (int i = 0; i < I; i++) acc += h[i] * ((double)ds[j] * e4m3_value(wd_q[(int64_t)j * I + i]));
+        y[j] = acc;
+    }
+    free(h);
+    return ORACLE_OK;
+}

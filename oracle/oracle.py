@@ -93,10 +93,13 @@ class Oracle:
         L.oracle_expert.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
         L.oracle_forward.argtypes = [cfgp, P, i64, P, i64, P, P, P, P, P, P, P, P, P, P]
         L.oracle_rmsnorm.argtypes = [ctypes.c_int, P, P, ctypes.c_double, P]
+        L.oracle_e4m3_decode.argtypes = [i64, P, P]
+        L.oracle_expert_fp8.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P]
         L.oracle_residual.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P]
         L.oracle_round_bf16.argtypes = [i64, P, P]
         for f in (L.oracle_check_cfg, L.oracle_router_logits, L.oracle_route, L.oracle_expert, L.oracle_forward,
-                  L.oracle_rmsnorm, L.oracle_residual, L.oracle_round_bf16):
+                  L.oracle_rmsnorm, L.oracle_residual, L.oracle_round_bf16, L.oracle_e4m3_decode,
+                  L.oracle_expert_fp8):
             f.restype = ctypes.c_int
         self.L = L
         self.path = path
@@ -230,6 +233,45 @@ class Oracle:
         return out, x_rows
 
 
+    def e4m3_decode(self, q) -> np.ndarray:
+        """FP64 values of FP8 E4M3 codes (uint8 array, any shape)."""
+        q = np.ascontiguousarray(q, dtype=np.uint8)
+        out = np.empty(q.shape, np.float64)
+        _check(self.L.oracle_e4m3_decode(q.size, _ptr(q), _ptr(out)), "e4m3_decode")
+        return out
+
+    def expert_fp8(self, shape, x_row, wg_q, gs, wu_q, us, wd_q, ds) -> np.ndarray:
+        """One SwiGLU expert with FP8 E4M3 weights and per-row FP32 scales on one FP64 row."""
+        x_row = np.ascontiguousarray(x_row, dtype=np.float64)
+        arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (wg_q, wu_q, wd_q)]
+        scs = [_f32(a) for a in (gs, us, ds)]
+        y = np.empty(shape.d, np.float64)
+        _check(self.L.oracle_expert_fp8(shape.d, shape.I, _ptr(x_row), _ptr(arrs[0]), _ptr(scs[0]), _ptr(arrs[1]),
+                                        _ptr(scs[1]), _ptr(arrs[2]), _ptr(scs[2]), _ptr(y)), "expert_fp8")
+        return y
+
+    def forward_fp8(self, shape, x_bits, bias, experts_q, tokens, logits=None, router_w=None, idx_in=None):
+        """The MoE block with FP8 experts for the rows `tokens`: the same routing as
+        forward() (from `logits` if given), experts evaluated by expert_fp8, weighted sum in
+        FP64 in slot order. experts_q: e -> (wg_q, gs, wu_q, us, wd_q, ds). idx_in replaces
+        the selection for the given rows (weights from the oracle's own sigmoid scores)."""
+        x_bits = _u16(x_bits)
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        lg = _f32(logits)[tokens] if logits is not None else self.router_logits(shape, x_bits[tokens], router_w)
+        idx, _, dbg = self.route(shape, lg, bias, debug=True)
+        w64 = dbg["w64"]
+        if idx_in is not None:
+            idx = np.asarray(idx_in, np.int32)
+            s = dbg["s"].astype(np.float64)
+            picked = np.take_along_axis(s, idx.astype(np.int64), axis=1)
+            w64 = shape.scale * picked / picked.sum(axis=1, keepdims=True)
+        out = np.zeros((len(tokens), shape.d), np.float64)
+        for n, t in enumerate(tokens):
+            xr = (x_bits[t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            for k in range(shape.top_k):
+                out[n] += w64[n, k] * self.expert_fp8(shape, xr, *experts_q(int(idx[n, k])))
+        return out, idx
+
     def forward_shard(self, shape, x_bits, bias, experts, e_begin, e_end, tokens, logits=None, router_w=None):
         """One expert-parallel shard's partial output for the rows `tokens`: the sum over the
         token's slots routed to experts [e_begin, e_end) of w_k * expert_k(x), FP64, with
@@ -291,6 +333,18 @@ def sublayer(*a, **k):
 
 def forward_shard(*a, **k):
     return default().forward_shard(*a, **k)
+
+
+def e4m3_decode(*a, **k):
+    return default().e4m3_decode(*a, **k)
+
+
+def expert_fp8(*a, **k):
+    return default().expert_fp8(*a, **k)
+
+
+def forward_fp8(*a, **k):
+    return default().forward_fp8(*a, **k)
 
 
 def bf16_bits(t) -> np.ndarray:

@@ -98,6 +98,37 @@ def make_experts(shape: MoEShape, seed: int = 0, device="cpu"):
     return tuple(out)
 
 
+FP8_MAX = 448.0  # largest finite FP8 E4M3 value
+
+
+def quantize_rows_fp8(w: torch.Tensor):
+    """Weight-only FP8 checkpoint recipe (the pages ship FP8 checkpoints but give no recipe;
+    this is the plainest per-row one): per output row r, scale[r] = max|w[r]| / 448 (FP32)
+    and q[r] = w[r] / scale[r] rounded to E4M3 by torch. Returns (q as uint8, scale)."""
+    wf = w.float()
+    scale = wf.abs().amax(dim=-1).clamp_min(1e-30) / FP8_MAX
+    q = (wf / scale.unsqueeze(-1)).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), scale
+
+
+def make_experts_fp8(shape: MoEShape, seed: int = 0, device="cpu"):
+    """The experts of make_experts (same draws), quantised per row with quantize_rows_fp8:
+    ((wg_q, wg_scale), (wu_q, wu_scale), (wd_q, wd_scale)) with q uint8 [E, rows, cols] and
+    scale float32 [E, rows]. Built one expert at a time (peak extra memory: one expert)."""
+    E, d, I = shape.E, shape.d, shape.I
+    out = []
+    for tag, rows, fan_in in (("w_gate", I, d), ("w_up", I, d), ("w_down", d, I)):
+        g = generator(seed, tag, device)
+        q = torch.empty((E, rows, fan_in), device=device, dtype=torch.uint8)
+        sc = torch.empty((E, rows), device=device, dtype=torch.float32)
+        std = 1.0 / math.sqrt(fan_in)
+        for e in range(E):
+            w = torch.randn((rows, fan_in), generator=g, device=device, dtype=torch.float32).mul_(std)
+            q[e], sc[e] = quantize_rows_fp8(w.to(torch.bfloat16))
+        out.append((q, sc))
+    return tuple(out)
+
+
 def sample_tokens(T: int, n: int, seed: int = 0) -> torch.Tensor:
     """A seeded, sorted subset of n distinct token indices out of T (all of them if n >= T)."""
     if n >= T:

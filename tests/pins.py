@@ -323,11 +323,39 @@ def pin_sublayer_composition(O, seed=15):
     np.testing.assert_allclose(out, want.numpy(), rtol=1e-9, atol=1e-9)
 
 
+def pin_e4m3_decoder_vs_torch(O):
+    """Every FP8 E4M3 code decodes to torch's float8_e4m3fn value (NaN codes to NaN)."""
+    q = np.arange(256, dtype=np.uint8)
+    got = O.e4m3_decode(q)
+    want = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    np.testing.assert_array_equal(got[~np.isnan(got)], want[~np.isnan(want)])
+
+
+def pin_fp8_expert_vs_torch(O, seed=16):
+    """The FP8 expert equals the BF16-free SwiGLU of torch float64 on the dequantised
+    weights (per-row scale times the E4M3 value), for the quantised Tiny experts."""
+    shape = W.TINY
+    (gq, gs), (uq, us), (dq, ds) = W.make_experts_fp8(shape, seed)
+    e = 5
+    deq = lambda q, sc: torch.from_numpy(O.e4m3_decode(q[e].numpy())) * sc[e].double().unsqueeze(1)  # noqa: E731
+    wg64, wu64, wd64 = deq(gq, gs), deq(uq, us), deq(dq, ds)
+    x = torch.randn(shape.d, generator=torch.Generator().manual_seed(seed), dtype=torch.float64)
+    got = O.expert_fp8(shape, x.numpy(), gq[e].numpy(), gs[e].numpy(), uq[e].numpy(), us[e].numpy(), dq[e].numpy(),
+                       ds[e].numpy())
+    want = (torch.nn.functional.silu(wg64 @ x) * (wu64 @ x)) @ wd64.T
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-10, atol=1e-12)
+    # and the quantisation is close to the BF16 expert it came from (a sanity bound)
+    wg, wu, wd = (w[e].double() for w in W.make_experts(shape, seed))
+    ref = (torch.nn.functional.silu(wg @ x) * (wu @ x)) @ wd.T
+    assert float((want - ref).norm() / ref.norm()) < 0.08
+
+
 ALL_CHECKS = [
     check_golden_cases, check_invariants, check_sigmoid_and_bias, check_group_scores_vs_topk,
     check_group_choice_brute_force, check_selection_brute_force_small, check_plain_topk_reduction,
     check_logits_vs_matmul, check_expert_vs_torch, check_forward_combination, check_zero_input,
     check_identical_experts, check_given_selection,
     pin_rmsnorm_library, pin_rmsnorm_closed_forms, pin_residual_is_scaled_sum, pin_round_bf16_vs_torch,
-    pin_sublayer_composition,
+    pin_sublayer_composition, pin_e4m3_decoder_vs_torch, pin_fp8_expert_vs_torch,
 ]

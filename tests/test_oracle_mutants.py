@@ -35,6 +35,13 @@ MUTANTS = [
     ("rmsnorm_eps_dropped", "1.0 / sqrt(ss / (double)d + eps)", "1.0 / sqrt(ss / (double)d)"),
     ("rmsnorm_gain_dropped", "y[j] = bf16_value(gamma[j]) * v[j] * r;", "y[j] = v[j] * r;"),
     ("bf16_truncates", "double r = nearbyint(ldexp(m, 8));", "double r = trunc(ldexp(m, 8));"),
+    ("e4m3_bias_off_by_one", "else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3_subnormal_scale", "if (e == 0) v = ldexp((double)m / 8.0, -6);", "if (e == 0) v = ldexp((double)m / 8.0, -7);"),
+    ("fp8_down_scale_dropped", "acc += h[i] * ((double)ds[j] * e4m3_value(wd_q[(int64_t)j * I + i]));",
+     "acc += h[i] * e4m3_value(wd_q[(int64_t)j * I + i]);"),
+    ("fp8_silu_on_up", "h[i] = g * u / (1.0 + exp(-g));", "h[i] = g * u / (1.0 + exp(-u));"),
+    ("fp8_up_scale_from_gate", "u += x[j] * ((double)us[i] * e4m3_value(wu_q[(int64_t)i * d + j]));",
+     "u += x[j] * ((double)gs[i] * e4m3_value(wu_q[(int64_t)i * d + j]));"),
 ]
 
 
