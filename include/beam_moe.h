@@ -100,8 +100,8 @@ BEAM_MOE_API int beam_moe_route_ex(const beam_moe_config *cfg, const __nv_bfloat
  *   w_down        bf16 [E, d, I]
  *   out           bf16 [T, d]
  * Numerics: FP32 router; BF16 tensor-core products with FP32 accumulation; SwiGLU in FP32,
- * its result rounded to BF16 for the down product; FP32 down outputs combined in FP32 in
- * slot order, rounded once to BF16.
+ * its result rounded to BF16 for the down product; each expert's output rounded to BF16 (the
+ * model's dtype), the weighted combine summed in FP32 in slot order and rounded once to BF16.
  * beam_moe_forward uses Beam's shape. */
 BEAM_MOE_API int beam_moe_forward(const __nv_bfloat16 *x, const float *router_w, const float *expert_bias,
                      const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up, const __nv_bfloat16 *w_down, int T,
@@ -109,6 +109,25 @@ BEAM_MOE_API int beam_moe_forward(const __nv_bfloat16 *x, const float *router_w,
 BEAM_MOE_API int beam_moe_forward_ex(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
                         const float *expert_bias, const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up,
                         const __nv_bfloat16 *w_down, int T, __nv_bfloat16 *out, cudaStream_t stream);
+
+/* Whole MoE block with FP8 expert weights. The pages ship FP8 (and NVFP4) checkpoints of the
+ * model (Glonce "Reflection releases Beam ...", Hardware paragraph; transformers "Beam" doc,
+ * checkpoint formats) but give no quantisation recipe; this call takes the plainest
+ * weight-only reading: FP8 E4M3 codes (bit 7 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; 0x7F/0xFF are NaN and must not occur) with one FP32 scale per output row,
+ *   Wg[e][i][j] = gate_scale[e][i] * e4m3(w_gate_q[e][i][j])      w_gate_q, w_up_q u8 [E, I, d]
+ *   Wu[e][i][j] = up_scale[e][i]   * e4m3(w_up_q[e][i][j])        gate_scale, up_scale f32 [E, I]
+ *   Wd[e][j][i] = down_scale[e][j] * e4m3(w_down_q[e][j][i])      w_down_q u8 [E, d, I], down_scale f32 [E, d]
+ * and otherwise the block of beam_moe_forward_ex: same routing, activations and output in
+ * BF16. Numerics: the codes are widened to BF16 exactly on chip, the products run on the
+ * BF16 tensor cores with FP32 accumulation, and each accumulator is multiplied by its row's
+ * scale in FP32 before SwiGLU (gate/up) or before rounding the expert output (down). All
+ * pointers are device memory, 16-byte aligned, owned by the caller and only read (out is
+ * written); errors as for beam_moe_forward_ex. */
+BEAM_MOE_API int beam_moe_forward_fp8(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
+                         const float *expert_bias, const uint8_t *w_gate_q, const float *gate_scale,
+                         const uint8_t *w_up_q, const float *up_scale, const uint8_t *w_down_q,
+                         const float *down_scale, int T, __nv_bfloat16 *out, cudaStream_t stream);
 
 /* One expert-parallel shard of the MoE block. The pages' multi-GPU plan puts each expert on
  * one device and replicates the rest, with a device count that divides 256 (Glonce "Reflection

@@ -8,7 +8,7 @@ from . import workloads  # noqa: F401
 from .abi import (  # noqa: F401
     BeamMoeConfig, BeamMoeError, beam_moe_default_config, beam_moe_dense_mlp, beam_moe_device_status,
     beam_moe_forward,
-    beam_moe_forward_ex, beam_moe_forward_shard, beam_moe_last_error, beam_moe_last_launch_count, beam_moe_route, beam_moe_route_ex,
+    beam_moe_forward_ex, beam_moe_forward_fp8, beam_moe_forward_shard, beam_moe_last_error, beam_moe_last_launch_count, beam_moe_route, beam_moe_route_ex,
     beam_moe_rmsnorm, beam_moe_route_noalloc, beam_moe_router_logits, beam_moe_sublayer_forward,
     beam_moe_timing_enable, beam_moe_timing_read,
 )

@@ -215,10 +215,12 @@ struct ShardArgs {
 // mode 0: route (outputs topk_idx/topk_w); 1: logits only; 2: forward; 3: sublayer (x is
 // the residual stream: pre-norm, forward, then combine fused with the post-norm and the
 // residual update into out); 4: forward of one expert-parallel shard (wg/wu/wd hold only
-// experts [e_begin, e_end); FP32 partial output over the slots routed there).
+// experts [e_begin, e_end); FP32 partial output over the slots routed there); 5: forward
+// with FP8 expert weights (q8; wg/wu/wd unused).
 int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float* bias, const bf16* wg,
         const bf16* wu, const bf16* wd, int T, int32_t* topk_idx, float* topk_w, float* logits, bf16* out, int mode,
-        cudaStream_t st, const SublayerArgs* sub = nullptr, const ShardArgs* shard = nullptr) {
+        cudaStream_t st, const SublayerArgs* sub = nullptr, const ShardArgs* shard = nullptr,
+        const Fp8Experts* q8 = nullptr) {
     g_launches = 0;
     timing_begin_call();
     int rc;
@@ -234,8 +236,15 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     if (mode != 1 && (rc = check_ptr(bias, "expert_bias"))) return rc;
     if (mode == 0 && ((rc = check_ptr(topk_idx, "topk_idx")) || (rc = check_ptr(topk_w, "topk_w")))) return rc;
     if (mode == 1 && (rc = check_ptr(logits, "logits"))) return rc;
-    if (mode >= 2 && ((rc = check_ptr(wg, "w_gate")) || (rc = check_ptr(wu, "w_up")) || (rc = check_ptr(wd, "w_down"))))
+    if (mode == 5) {
+        if ((rc = check_ptr(q8->wg, "w_gate_q")) || (rc = check_ptr(q8->gs, "gate_scale")) ||
+            (rc = check_ptr(q8->wu, "w_up_q")) || (rc = check_ptr(q8->us, "up_scale")) ||
+            (rc = check_ptr(q8->wd, "w_down_q")) || (rc = check_ptr(q8->ds, "down_scale")))
+            return rc;
+    } else if (mode >= 2 &&
+               ((rc = check_ptr(wg, "w_gate")) || (rc = check_ptr(wu, "w_up")) || (rc = check_ptr(wd, "w_down")))) {
         return rc;
+    }
     if (mode == 4) {
         if ((rc = check_ptr(shard->out_partial, "out_partial"))) return rc;
         if (shard->e_begin < 0 || shard->e_begin >= shard->e_end || shard->e_end > cfg->E)
@@ -275,7 +284,7 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     Shape se = s;
     se.E = mode == 4 ? shard->e_end - shard->e_begin : s.E;
     const RouterPlan plan = router_plan(s, T, dev->num_sms);
-    const int bn_max = gemm_bn_max(s, T);
+    const int bn_max = mode == 5 ? gemm_bn_max_fp8(s, T) : gemm_bn_max(s, T);
     const int max_tiles = dispatch_max_tiles(se, T, bn_max);
     const int rows = T * s.top_k;
     Scratch sc;
@@ -304,8 +313,12 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
                                                      dev->status, st));
             LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
                                                dev->status, dev->num_sms, st));
-            LAUNCH(kExpert, launch_expert_mlp(se, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
-                                              bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
+            if (mode == 5)
+                LAUNCH(kExpert, launch_expert_mlp_fp8(se, *q8, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
+                                                      bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
+            else
+                LAUNCH(kExpert, launch_expert_mlp(se, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done,
+                                                  max_tiles, bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
             if (mode == 4)
                 LAUNCH(kCombine, launch_combine_partial(s, sc.y, sc.inv_slot, w, T, shard->out_partial, dev->status,
                                                         st));
@@ -397,6 +410,15 @@ int beam_moe_forward_shard(const beam_moe_config* cfg, const __nv_bfloat16* x, c
     const ShardArgs sh{e_begin, e_end, out_partial};
     return run(cfg, x, router_w, expert_bias, w_gate, w_up, w_down, T, nullptr, nullptr, nullptr, nullptr, 4, stream,
                nullptr, &sh);
+}
+
+int beam_moe_forward_fp8(const beam_moe_config* cfg, const __nv_bfloat16* x, const float* router_w,
+                         const float* expert_bias, const uint8_t* w_gate_q, const float* gate_scale,
+                         const uint8_t* w_up_q, const float* up_scale, const uint8_t* w_down_q,
+                         const float* down_scale, int T, __nv_bfloat16* out, cudaStream_t stream) {
+    const Fp8Experts q{w_gate_q, gate_scale, w_up_q, up_scale, w_down_q, down_scale};
+    return run(cfg, x, router_w, expert_bias, nullptr, nullptr, nullptr, T, nullptr, nullptr, nullptr, out, 5, stream,
+               nullptr, nullptr, &q);
 }
 
 int beam_moe_dense_mlp(int d, int I, const __nv_bfloat16* x, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,

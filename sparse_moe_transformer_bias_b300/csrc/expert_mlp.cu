@@ -40,6 +40,17 @@
 // Every wait is bounded (2 s); on expiry the CTA records kStatusWaitTimeout, the roles
 // leave their loops, copies and MMAs already issued are drained (bounded), and TMEM is
 // freed before the CTA exits.
+//
+// FP8 weights (kFP8): the weights are E4M3 codes with one FP32 scale per output row. TMA
+// streams the byte tiles [128 x 64] (64-byte swizzle) next to the BF16 token rows; eight
+// converter warps (two per TMEM lane quarter, one per weight tile of the stage) widen each
+// row's 64 codes and store them with tcgen05.st into a ring of A buffers in TMEM, and the
+// MMA reads A from TMEM (B, the token rows, still from shared memory). The widening is
+// exact: E4M3 -> F16 by cvt (every finite code is an F16 normal or zero), then F16 -> BF16
+// by moving the exponent and mantissa bits down three places, which keeps every bit and
+// multiplies the value by 2^-112 (zero stays zero; every nonzero code lands on a BF16
+// normal). The epilogue multiplies each accumulator by 2^112 and then by its row's scale,
+// so the products are those of W[r][c] = scale[r] * e4m3(q[r][c]) with FP32 accumulation.
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -47,30 +58,40 @@ namespace beam {
 namespace {
 
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kConvWarps = 8;  // FP8 weights: two converter warps per TMEM lane quarter
+constexpr int kThreadsFor(bool fp8) { return 64 + 32 * kEpiWarps + (fp8 ? 32 * kConvWarps : 0); }
 constexpr int kRing = 4;  // item ids in flight between the scheduler and the other roles
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-template <int kBNMax>
+template <int kBNMax, bool kFP8>
 struct MlpCfg {
-    static constexpr int kA = kTileM * kTileK * 2;
+    static constexpr int kThreads = kThreadsFor(kFP8);
+    static constexpr int kA = kTileM * kTileK * (kFP8 ? 1 : 2);  // one weight tile in shared memory
     static constexpr int kB = kBNMax * kTileK * 2;
     static constexpr int kStage = 2 * kA + kB;
     static constexpr int kBudget = 227 * 1024 - 2048;
     static constexpr int kStages = (kBudget / kStage) > 10 ? 10 : (kBudget / kStage);
-    static constexpr int kSlots = (512 / kBNMax) < 4 ? (512 / kBNMax) : 4;
-    static constexpr int kColsNeeded = kSlots * kBNMax;
+    // FP8: a ring of converted A buffers in TMEM, each the stage's two weight tiles as BF16
+    // (2 x 32 columns), after the accumulator slots.
+    static constexpr int kABufs = kFP8 ? 4 : 0;
+    static constexpr int kACols = 2 * kTileK / 2;
+    static constexpr int kAccCols = 512 - kABufs * kACols;
+    static constexpr int kSlots = (kAccCols / kBNMax) < 4 ? (kAccCols / kBNMax) : 4;
+    static constexpr int kABase = kSlots * kBNMax;  // first TMEM column of the A buffers
+    static constexpr int kColsNeeded = kSlots * kBNMax + kABufs * kACols;
     static constexpr int kTmemCols = kColsNeeded <= 32    ? 32
                                      : kColsNeeded <= 64  ? 64
                                      : kColsNeeded <= 128 ? 128
                                      : kColsNeeded <= 256 ? 256
                                                           : 512;
-    // FULL, EMPTY per stage; TFULL, TEMPTY per slot; RFULL, REMPTY per ring entry; DRAIN.
-    static constexpr int kNumBars = 2 * kStages + 2 * kSlots + 2 * kRing + 1;
+    // FULL, EMPTY per stage; TFULL, TEMPTY per slot; RFULL, REMPTY per ring entry; DRAIN;
+    // AFULL, AEMPTY per A buffer.
+    static constexpr int kNumBars = 2 * kStages + 2 * kSlots + 2 * kRing + 1 + 2 * kABufs;
     static constexpr int kSmemBytes = 1024 + kStages * kStage + kNumBars * 8 + kRing * 4 + 16;
     static_assert(kStages >= 2, "pipeline needs two stages");
-    static_assert(kSlots >= 2, "a gate/up item needs two accumulator slots");
+    static_assert(kSlots >= 2 && kSlots % 2 == 0, "an item takes two accumulator slots");
+    static_assert(kColsNeeded <= 512 && kABase + kABufs * kACols <= 512, "TMEM columns");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -86,6 +107,9 @@ struct MlpArgs {
     int I, d;
     bf16* h;
     bf16* y;             // [rows, d] expert outputs (the dense MLP: its output)
+    const float* gs;     // FP8 weights: per-row scales of Wg, Wu [E, I] and Wd [E, d]
+    const float* us;
+    const float* ds;
     int* status;
 };
 
@@ -136,12 +160,25 @@ __device__ bool wait_counter(const int* counter, int need, const volatile int* a
     }
 }
 
-template <int kBNMax>
-__global__ void __launch_bounds__(kThreads, 1)
+// Four E4M3 codes (bytes k..k+3 of w, k first) -> two words of two BF16 each (element k in
+// the lower half), every value times 2^-112 exactly. cvt gives the F16 pair; an F16 that
+// comes from E4M3 has its three lowest mantissa bits zero, so one shift of the word moves
+// both halves' exponent and mantissa fields into BF16 position without mixing them.
+__device__ __forceinline__ void e4m3x4_to_bf16x4_scaled(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    uint32_t f0, f1;
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+        : "=r"(f0), "=r"(f1)
+        : "r"(w));
+    lo = ((f0 & 0x7fff7fffu) >> 3) | (f0 & 0x80008000u);
+    hi = ((f1 & 0x7fff7fffu) >> 3) | (f1 & 0x80008000u);
+}
+
+template <int kBNMax, bool kFP8>
+__global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
     expert_mlp_kernel(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ CUtensorMap tmWu,
                       const __grid_constant__ CUtensorMap tmWd, const __grid_constant__ BMaps tmX,
                       const __grid_constant__ BMaps tmH, const __grid_constant__ MlpArgs args) {
-    using C = MlpCfg<kBNMax>;
+    using C = MlpCfg<kBNMax, kFP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
@@ -149,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kRing);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     constexpr int FULL0 = 0, EMPTY0 = C::kStages, TFULL0 = 2 * C::kStages, TEMPTY0 = TFULL0 + C::kSlots,
-                  RFULL0 = TEMPTY0 + C::kSlots, REMPTY0 = RFULL0 + kRing, DRAIN = REMPTY0 + kRing;
+                  RFULL0 = TEMPTY0 + C::kSlots, REMPTY0 = RFULL0 + kRing, DRAIN = REMPTY0 + kRing,
+                  AFULL0 = DRAIN + 1, AEMPTY0 = AFULL0 + C::kABufs;
     auto bar = [&](int i) { return ptx::smem_u32(bars + i); };
     int* status = args.status;
 
@@ -157,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(bar(FULL0 + s), 1);
-            ptx::mbar_init(bar(EMPTY0 + s), 1);
+            ptx::mbar_init(bar(EMPTY0 + s), kFP8 ? 1 + kConvWarps : 1);  // FP8: converters read it too
         }
         for (int s = 0; s < C::kSlots; ++s) {
             ptx::mbar_init(bar(TFULL0 + s), 1);
@@ -165,9 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int r = 0; r < kRing; ++r) {
             ptx::mbar_init(bar(RFULL0 + r), 1);
-            ptx::mbar_init(bar(REMPTY0 + r), 1 + kEpiWarps);
+            ptx::mbar_init(bar(REMPTY0 + r), 1 + kEpiWarps + (kFP8 ? kConvWarps : 0));
         }
         ptx::mbar_init(bar(DRAIN), 1);
+        for (int b = 0; b < C::kABufs; ++b) {
+            ptx::mbar_init(bar(AFULL0 + b), kConvWarps);
+            ptx::mbar_init(bar(AEMPTY0 + b), 1);
+        }
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -283,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
-            int stage = 0, rslot = 0, slot = 0;
-            uint32_t phase = 0, rphase = 0, tph = 0;  // tph bit s: parity of slot s's current use
+            int stage = 0, rslot = 0, slot = 0, abuf = 0;
+            uint32_t phase = 0, rphase = 0, tph = 0, aphase = 0;  // tph bit s: parity of slot s's current use
             bool ok = true;
             while (ok) {
                 if (!ptx::mbar_wait(bar(RFULL0 + rslot), rphase, abort_flag, kWaitLimitNs)) {
@@ -315,6 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    if constexpr (kFP8) {
+                        if (!ptx::mbar_wait(bar(AFULL0 + abuf), aphase, abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_u32(smem + stage * C::kStage);
                     const uint32_t sb = sa + 2 * C::kA;
@@ -322,10 +370,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
                         const uint64_t bdesc = ptx::sw128_kmajor_desc(sb + kk * kMmaK * 2);
                         const uint32_t accum = (kc | kk) ? 1u : 0u;
-                        ptx::mma_bf16(d0, ptx::sw128_kmajor_desc(sa + kk * kMmaK * 2), bdesc, idesc, accum);
-                        ptx::mma_bf16(d1, ptx::sw128_kmajor_desc(sa + C::kA + kk * kMmaK * 2), bdesc, idesc, accum);
+                        if constexpr (kFP8) {
+                            const uint32_t ta = tmem_base + C::kABase + abuf * C::kACols + kk * (kMmaK / 2);
+                            ptx::mma_bf16_ta(d0, ta, bdesc, idesc, accum);
+                            ptx::mma_bf16_ta(d1, ta + kTileK / 2, bdesc, idesc, accum);
+                        } else {
+                            ptx::mma_bf16(d0, ptx::sw128_kmajor_desc(sa + kk * kMmaK * 2), bdesc, idesc, accum);
+                            ptx::mma_bf16(d1, ptx::sw128_kmajor_desc(sa + C::kA + kk * kMmaK * 2), bdesc, idesc,
+                                          accum);
+                        }
                     }
                     ptx::mma_commit(bar(EMPTY0 + stage));
+                    if constexpr (kFP8) {
+                        ptx::mma_commit(bar(AEMPTY0 + abuf));
+                        if (++abuf == C::kABufs) {
+                            abuf = 0;
+                            aphase ^= 1;
+                        }
+                    }
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -343,6 +405,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int never = 0;
                 ptx::mma_commit(bar(DRAIN));
                 ptx::mbar_wait(bar(DRAIN), 0, &never, kDrainLimitNs);
+            }
+        }
+    } else if (warp >= 2 + kEpiWarps) {
+        if constexpr (kFP8) {
+            // ------------------------------------------------------------ FP8 -> BF16 converters
+            // Warp pair per lane quarter: weight tile t (gate or the even Wd tile: 0; up or
+            // the odd Wd tile: 1) of every stage, one weight row per thread.
+            const int q = warp & 3;
+            const int t = (warp - 2 - kEpiWarps) >> 2;
+            const int r = q * 32 + lane;
+            const int swz = (r >> 1) & 3;  // the 64-byte swizzle of the byte tile
+            const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+            int stage = 0, rslot = 0, abuf = 0;
+            uint32_t phase = 0, rphase = 0, aphase = 0;
+            bool ok = true;
+            while (ok) {
+                if (!ptx::mbar_wait(bar(RFULL0 + rslot), rphase, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                const int id = ring[rslot];
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(REMPTY0 + rslot));
+                if (++rslot == kRing) {
+                    rslot = 0;
+                    rphase ^= 1;
+                }
+                if (id < 0) break;
+                const MItem it = decode(args, id, n_gu);
+                if (!it.ok || it.tl.z > kBNMax) continue;
+                const int k_chunks = it.down ? args.kc_dn : args.kc_gu;
+                for (int kc = 0; kc < k_chunks; ++kc) {
+                    if (!ptx::mbar_wait(bar(FULL0 + stage), phase, abort_flag, kWaitLimitNs) ||
+                        !ptx::mbar_wait(bar(AEMPTY0 + abuf), aphase ^ 1, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint8_t* src = smem + stage * C::kStage + t * C::kA + r * kTileK;
+                    uint4 v[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(src + 16 * (j ^ swz));
+                    uint32_t o[32];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        e4m3x4_to_bf16x4_scaled(v[j].x, o[8 * j + 0], o[8 * j + 1]);
+                        e4m3x4_to_bf16x4_scaled(v[j].y, o[8 * j + 2], o[8 * j + 3]);
+                        e4m3x4_to_bf16x4_scaled(v[j].z, o[8 * j + 4], o[8 * j + 5]);
+                        e4m3x4_to_bf16x4_scaled(v[j].w, o[8 * j + 6], o[8 * j + 7]);
+                    }
+                    ptx::tmem_st32(tmem_base + lane_off + C::kABase + abuf * C::kACols + t * (kTileK / 2), o);
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::mbar_arrive(bar(AFULL0 + abuf));
+                        ptx::mbar_arrive(bar(EMPTY0 + stage));
+                    }
+                    if (++abuf == C::kABufs) {
+                        abuf = 0;
+                        aphase ^= 1;
+                    }
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                flag_status(status, kStatusWaitTimeout);
             }
         }
     } else {
@@ -381,6 +514,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t t0 = tmem_base + lane_off + s0 * kBNMax, t1 = tmem_base + lane_off + s1 * kBNMax;
             const int col = (it.down ? it.m * 2 * kTileM : it.m * kTileM) + row;
             const bool col1_ok = col + kTileM < args.d;  // down: the pair's second tile exists
+            // FP8: the row scales of this thread's weight row(s), the 2^112 of the widening
+            // applied first (exact)
+            float sc0 = 1.0f, sc1 = 1.0f;
+            if constexpr (kFP8) {
+                if (!it.down) {
+                    sc0 = args.gs[static_cast<size_t>(it.tl.x) * args.I + col];
+                    sc1 = args.us[static_cast<size_t>(it.tl.x) * args.I + col];
+                } else {
+                    sc0 = args.ds[static_cast<size_t>(it.tl.x) * args.d + col];
+                    sc1 = col1_ok ? args.ds[static_cast<size_t>(it.tl.x) * args.d + col + kTileM] : 0.0f;
+                }
+            }
+            constexpr float kP112 = 5.192296858534828e33f;  // 2^112
             for (int c0 = col_part * 16; c0 < it.tl.z; c0 += kColStep) {
                 uint32_t g[16];
                 ptx::tmem_ld16(t0 + c0, g);
@@ -391,8 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < it.tl.z) {
-                            const float gv = __uint_as_float(g[j]);
-                            const float uv = __uint_as_float(u[j]);
+                            float gv = __uint_as_float(g[j]);
+                            float uv = __uint_as_float(u[j]);
+                            if constexpr (kFP8) {
+                                gv = (gv * kP112) * sc0;
+                                uv = (uv * kP112) * sc1;
+                            }
                             // silu(g) * u in FP32 with the fast exponential and division
                             // (a few ulp; the result is rounded to BF16 next)
                             const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
@@ -407,8 +557,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < it.tl.z) {
                             const size_t r0 = static_cast<size_t>(it.tl.y + c0 + j) * args.d;
-                            args.y[r0 + col] = __float2bfloat16_rn(__uint_as_float(g[j]));
-                            if (col1_ok) args.y[r0 + col + kTileM] = __float2bfloat16_rn(__uint_as_float(g1[j]));
+                            float y0 = __uint_as_float(g[j]), y1 = __uint_as_float(g1[j]);
+                            if constexpr (kFP8) {
+                                y0 = (y0 * kP112) * sc0;
+                                y1 = (y1 * kP112) * sc1;
+                            }
+                            args.y[r0 + col] = __float2bfloat16_rn(y0);
+                            if (col1_ok) args.y[r0 + col + kTileM] = __float2bfloat16_rn(y1);
                         }
                     }
                 }
@@ -441,14 +596,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int kBNMax>
+template <int kBNMax, bool kFP8>
 cudaError_t launch_mlp(const CUtensorMap& wg, const CUtensorMap& wu, const CUtensorMap& wd, const BMaps& x,
                        const BMaps& h, const MlpArgs& args, int grid, cudaStream_t st) {
-    using C = MlpCfg<kBNMax>;
-    auto kern = expert_mlp_kernel<kBNMax>;
+    using C = MlpCfg<kBNMax, kFP8>;
+    auto kern = expert_mlp_kernel<kBNMax, kFP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const cudaError_t le_ = launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, st, wg, wu, wd, x, h, args);
+    const cudaError_t le_ =
+        launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, wg, wu, wd, x, h, args);
     if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
@@ -463,6 +619,11 @@ int gemm_bn_max(const Shape& s, int T) {
     if (T <= 32) return 32;
     const long long avg_rows = static_cast<long long>(T) * s.top_k / s.E;
     return avg_rows <= 32 ? 128 : 256;
+}
+
+int gemm_bn_max_fp8(const Shape& s, int T) {
+    const int b = gemm_bn_max(s, T);
+    return b < 128 ? b : 128;
 }
 
 namespace {
@@ -493,18 +654,10 @@ cudaError_t launch_dense_tiles(int T, int bn_max, int4* tiles, int* tile_done, c
     return cudaGetLastError();
 }
 
-cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* w_down,
-                              const bf16* x_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
-                              int bn_max, bf16* h, bf16* y, int* status, int num_sms,
-                              cudaStream_t st) {
-    CUtensorMap wg, wu, wd;
-    BMaps bx, bh;
-    const char* why = nullptr;
-    if (!encode_tmap_bf16_2d(&wg, w_gate, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kTileK, &why) ||
-        !encode_tmap_bf16_2d(&wu, w_up, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kTileK, &why) ||
-        !encode_tmap_bf16_2d(&wd, w_down, static_cast<uint64_t>(s.E) * s.d, s.I, kTileM, kTileK, &why) ||
-        !encode_bmaps(&bx, x_perm, rows, s.d, bn_max, &why) || !encode_bmaps(&bh, h, rows, s.I, bn_max, &why))
-        return cudaErrorInvalidValue;
+namespace {
+
+MlpArgs mlp_args(const Shape& s, int rows, const int4* tiles, int* tile_done, int max_tiles, bf16* h, bf16* y,
+                 int* status) {
     MlpArgs a;
     a.tiles = tiles;
     a.next_item = const_cast<int*>(reinterpret_cast<const int*>(tiles)) + 1;
@@ -520,12 +673,56 @@ cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_
     a.d = s.d;
     a.h = h;
     a.y = y;
+    a.gs = a.us = a.ds = nullptr;
     a.status = status;
+    return a;
+}
+
+int mlp_grid(const MlpArgs& a, int max_tiles, int num_sms) {
     const long long items = static_cast<long long>(max_tiles) * (a.m_gu + a.m_dn);
-    const int grid = static_cast<int>(items < num_sms ? (items < 1 ? 1 : items) : num_sms);
-    if (bn_max <= 32) return launch_mlp<32>(wg, wu, wd, bx, bh, a, grid, st);
-    if (bn_max <= 128) return launch_mlp<128>(wg, wu, wd, bx, bh, a, grid, st);
-    return launch_mlp<256>(wg, wu, wd, bx, bh, a, grid, st);
+    return static_cast<int>(items < num_sms ? (items < 1 ? 1 : items) : num_sms);
+}
+
+}  // namespace
+
+cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_up, const bf16* w_down,
+                              const bf16* x_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
+                              int bn_max, bf16* h, bf16* y, int* status, int num_sms,
+                              cudaStream_t st) {
+    CUtensorMap wg, wu, wd;
+    BMaps bx, bh;
+    const char* why = nullptr;
+    if (!encode_tmap_bf16_2d(&wg, w_gate, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kTileK, &why) ||
+        !encode_tmap_bf16_2d(&wu, w_up, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kTileK, &why) ||
+        !encode_tmap_bf16_2d(&wd, w_down, static_cast<uint64_t>(s.E) * s.d, s.I, kTileM, kTileK, &why) ||
+        !encode_bmaps(&bx, x_perm, rows, s.d, bn_max, &why) || !encode_bmaps(&bh, h, rows, s.I, bn_max, &why))
+        return cudaErrorInvalidValue;
+    const MlpArgs a = mlp_args(s, rows, tiles, tile_done, max_tiles, h, y, status);
+    const int grid = mlp_grid(a, max_tiles, num_sms);
+    if (bn_max <= 32) return launch_mlp<32, false>(wg, wu, wd, bx, bh, a, grid, st);
+    if (bn_max <= 128) return launch_mlp<128, false>(wg, wu, wd, bx, bh, a, grid, st);
+    return launch_mlp<256, false>(wg, wu, wd, bx, bh, a, grid, st);
+}
+
+cudaError_t launch_expert_mlp_fp8(const Shape& s, const Fp8Experts& q, const bf16* x_perm, int rows,
+                                  const int4* tiles, int* tile_done, int max_tiles, int bn_max, bf16* h, bf16* y,
+                                  int* status, int num_sms, cudaStream_t st) {
+    if (bn_max > 128) return cudaErrorInvalidValue;
+    CUtensorMap wg, wu, wd;
+    BMaps bx, bh;
+    const char* why = nullptr;
+    if (!encode_tmap_u8_2d(&wg, q.wg, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kTileK, &why) ||
+        !encode_tmap_u8_2d(&wu, q.wu, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kTileK, &why) ||
+        !encode_tmap_u8_2d(&wd, q.wd, static_cast<uint64_t>(s.E) * s.d, s.I, kTileM, kTileK, &why) ||
+        !encode_bmaps(&bx, x_perm, rows, s.d, bn_max, &why) || !encode_bmaps(&bh, h, rows, s.I, bn_max, &why))
+        return cudaErrorInvalidValue;
+    MlpArgs a = mlp_args(s, rows, tiles, tile_done, max_tiles, h, y, status);
+    a.gs = q.gs;
+    a.us = q.us;
+    a.ds = q.ds;
+    const int grid = mlp_grid(a, max_tiles, num_sms);
+    if (bn_max <= 32) return launch_mlp<32, true>(wg, wu, wd, bx, bh, a, grid, st);
+    return launch_mlp<128, true>(wg, wu, wd, bx, bh, a, grid, st);
 }
 
 }  // namespace beam

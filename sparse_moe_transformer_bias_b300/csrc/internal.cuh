@@ -94,6 +94,24 @@ cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_
                               const bf16* x_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
                               int bn_max, bf16* h, bf16* y, int* status, int num_sms,
                               cudaStream_t st);
+// FP8 E4M3 expert weights, one FP32 scale per output row: W[r][c] = scale[r] * e4m3(q[r][c]).
+// wg, wu [E, I, d] with gs, us [E, I]; wd [E, d, I] with ds [E, d].
+struct Fp8Experts {
+    const uint8_t* wg;
+    const float* gs;
+    const uint8_t* wu;
+    const float* us;
+    const uint8_t* wd;
+    const float* ds;
+};
+// Largest N-tile of the FP8 expert kernel (its converted weights share TMEM with the
+// accumulators, so tiles stop at 128 rows).
+int gemm_bn_max_fp8(const Shape& s, int T);
+// The expert kernel on FP8 weights: the same items and outputs as launch_expert_mlp, the
+// weight tiles widened to BF16 on chip and the accumulators scaled per weight row.
+cudaError_t launch_expert_mlp_fp8(const Shape& s, const Fp8Experts& q, const bf16* x_perm, int rows,
+                                  const int4* tiles, int* tile_done, int max_tiles, int bn_max, bf16* h, bf16* y,
+                                  int* status, int num_sms, cudaStream_t st);
 // Dense MLP (one "expert", every token in order): the work list and its capacity.
 int dense_max_tiles(int T, int bn_max);
 cudaError_t launch_dense_tiles(int T, int bn_max, int4* tiles, int* tile_done, cudaStream_t st);
@@ -151,5 +169,11 @@ bool encode_bmaps(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int 
 // swizzle and a box of box_cols x box_rows. Returns false if the driver refuses it.
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                          uint32_t box_cols, const char** why);
+
+// Host helper: encode a 2-D byte tensor map (FP8 codes, rows x cols, row-major) with the
+// 64-byte swizzle: in shared memory the 16-byte chunk c of row r of a 64-byte-wide box sits
+// at chunk c ^ ((r >> 1) & 3).
+bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                       uint32_t box_cols, const char** why);
 
 }  // namespace beam

@@ -1,5 +1,6 @@
 // Host helpers for the TMA tensor maps of the tcgen05 kernels (router_gemm.cu,
-// expert_mlp.cu): BF16 row-major matrices, 128-byte swizzle, boxes of 64 columns.
+// expert_mlp.cu): BF16 row-major matrices with the 128-byte swizzle, and FP8 (byte)
+// matrices with the 64-byte swizzle, boxes of 64 columns.
 #include <mutex>
 
 #include "internal.cuh"
@@ -42,6 +43,27 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *why = "cuTensorMapEncodeTiled rejected a tensor map";
+        return false;
+    }
+    return true;
+}
+
+bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                       uint32_t box_cols, const char** why) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        *why = "driver entry point cuTensorMapEncodeTiled is not available";
+        return false;
+    }
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *why = "cuTensorMapEncodeTiled rejected a tensor map";
         return false;

@@ -52,6 +52,22 @@ def forward(x, router_w, bias, w_gate, w_up, w_down, shape: MoEShape = BEAM, out
     return out
 
 
+def forward_fp8(x, router_w, bias, experts_fp8, shape: MoEShape = BEAM, out=None, stream=None):
+    """The block with FP8 E4M3 expert weights: experts_fp8 = ((wg_q, gs), (wu_q, us), (wd_q, ds))
+    with codes uint8 [E, I, d], [E, I, d], [E, d, I] and FP32 row scales [E, I], [E, I], [E, d]
+    (workloads.make_experts_fp8 builds them)."""
+    T = _check_inputs(shape, x, router_w, bias)
+    (wg, gs), (wu, us), (wd, ds) = experts_fp8
+    for (w, sc), rows, cols in (((wg, gs), shape.I, shape.d), ((wu, us), shape.I, shape.d),
+                                ((wd, ds), shape.d, shape.I)):
+        assert w.dtype == torch.uint8 and w.shape == (shape.E, rows, cols) and w.is_contiguous()
+        assert sc.dtype == torch.float32 and sc.shape == (shape.E, rows) and sc.is_contiguous()
+    if out is None:
+        out = torch.empty((T, shape.d), dtype=torch.bfloat16, device=x.device)
+    abi.beam_moe_forward_fp8(shape, x, router_w, bias, wg, gs, wu, us, wd, ds, T, out, stream)
+    return out
+
+
 def forward_host(x_host, router_w, bias, w_gate, w_up, w_down, shape: MoEShape = BEAM, x_dev=None, out_dev=None,
                  out_host=None, stream=None):
     """Host tokens in, host output out: copies x to the device, runs the block, copies

@@ -120,3 +120,21 @@ def oracle_forward_for(layer: Layer, tokens, gpu_logits_full, gpu_idx_full):
                                logits=gpu_logits_full, idx_in=idx_in[flagged_local])
         out[flagged_local] = out2
     return out, tokens[flagged_local]
+
+
+def oracle_forward_fp8_for(shape, x, bias, experts_q, tokens, gpu_logits_full, gpu_idx_full):
+    """oracle_forward_for with FP8 experts (experts_q: e -> (wg_q, gs, wu_q, us, wd_q, ds) as
+    numpy arrays): the oracle's routing from the GPU's logits, near-tie tokens rerun on the
+    GPU's selection. Returns (out [n, d] FP64, flagged tokens among `tokens`)."""
+    tokens = np.asarray(tokens, np.int64)
+    b = bias.cpu().numpy()
+    _, _, dbg = O.route(shape, gpu_logits_full[tokens], b, debug=True)
+    flagged_local = near_tie_tokens(shape, dbg)
+    xb = O.bf16_bits(x)
+    out, _ = O.forward_fp8(shape, xb, b, experts_q, tokens, logits=gpu_logits_full)
+    if len(flagged_local):
+        idx_in = np.asarray(gpu_idx_full[tokens], np.int32)[flagged_local]
+        out2, _ = O.forward_fp8(shape, xb, b, experts_q, tokens[flagged_local], logits=gpu_logits_full,
+                                idx_in=idx_in)
+        out[flagged_local] = out2
+    return out, tokens[flagged_local]

@@ -111,3 +111,19 @@ def test_dense_mlp_arguments_checked(lib):
     assert f(512, 256, FAKE, None, FAKE, FAKE, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
     assert f(512, 256, FAKE, FAKE, FAKE, FAKE + 8, 4, FAKE, None) == abi.BEAM_MOE_ERR_ALIGN
     assert f(512, 256, FAKE, FAKE, FAKE, FAKE, 0, FAKE, None) == abi.BEAM_MOE_OK
+
+
+def test_forward_fp8_arguments_checked(lib):
+    f = lib.beam_moe_forward_fp8
+    cfg = ctypes.byref(cfg_of())
+    args = [FAKE] * 9
+    assert f(cfg, *args, 0, FAKE, None) == abi.BEAM_MOE_OK
+    for i, name in enumerate(["x", "router_w", "expert_bias", "w_gate_q", "gate_scale", "w_up_q", "up_scale",
+                              "w_down_q", "down_scale"]):
+        bad = list(args)
+        bad[i] = None
+        assert f(cfg, *bad, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG, name
+        assert name in abi.beam_moe_last_error()
+        bad[i] = FAKE + 4
+        assert f(cfg, *bad, 4, FAKE, None) == abi.BEAM_MOE_ERR_ALIGN, name
+    assert f(cfg, *args, 4, None, None) == abi.BEAM_MOE_ERR_ARG
