@@ -1,7 +1,7 @@
 """Benchmark of the Beam routed-MoE forward pass (libbeam_moe.so) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|tiny|T<n>]
-                    [--impl reference] [--no-secondary]
+                    [--impl reference] [--no-secondary] [--weights bf16|fp8]
 
 A step is one beam_moe_forward call over one batch of T tokens: router, dispatch,
 gate/up GEMM with SwiGLU, down GEMM, combine. Inputs and weights are synthetic, seeded,
@@ -13,7 +13,9 @@ time is the max over ranks.
 
 The default workload is Beam decode (T=16); one JSON line is printed by rank 0, carrying
 the dominant kernel's roofline, the CPU oracle's throughput on a bounded sample, the
-end-to-end number through host buffers, and a secondary prefill (T=4096) measurement.
+end-to-end number through host buffers, a secondary prefill (T=4096) measurement, and the
+same block on FP8 E4M3 expert weights (decode and prefill). --weights fp8 makes the FP8
+block the headline (used to profile it on smaller shapes).
 --impl reference times the CPU oracle itself as the reference arm.
 """
 from __future__ import annotations
@@ -133,28 +135,35 @@ def make_layer(shape, T, hot, device, experts=None, seed=0):
     return x, wr, b, experts
 
 
-def algorithmic(shape, T, n_touched, rows):
+def algorithmic(shape, T, n_touched, rows, fp8=False):
     """Algorithmic FLOPs and bytes of the whole layer and of the expert kernel (one launch:
-    gate/up + SwiGLU and down over the touched experts' weights)."""
+    gate/up + SwiGLU and down over the touched experts' weights). FP8 experts: one byte
+    per weight plus one FP32 scale per weight row."""
     d, I, E, K = shape.d, shape.I, shape.E, shape.top_k
+    w_bytes = n_touched * (3 * d * I + (2 * I + d) * 4) if fp8 else n_touched * 3 * d * I * 2
     layer_flops = T * (K * 3 * 2 * d * I + 2 * d * E)
-    layer_bytes = n_touched * 3 * d * I * 2 + E * d * 4 + E * 4 + 2 * T * d * 2 + T * K * 8
+    layer_bytes = w_bytes + E * d * 4 + E * 4 + 2 * T * d * 2 + T * K * 8
     # weights once; x_perm read, h written and read back, y (BF16) written
     mlp = {"flops": 2 * rows * d * I * 3,
-           "bytes": n_touched * 3 * I * d * 2 + rows * d * 2 + 2 * rows * I * 2 + rows * d * 2}
+           "bytes": w_bytes + rows * d * 2 + 2 * rows * I * 2 + rows * d * 2}
     return layer_flops, layer_bytes, {"expert_mlp": mlp}
 
 
-def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=True):
+def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=True, experts_fp8=None):
+    """Times beam_moe_forward (or, given experts_fp8, beam_moe_forward_fp8) on the workload."""
     x, wr, b, (wg, wu, wd) = make_layer(shape, T, hot, device, experts)
     out = torch.empty((T, shape.d), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.current_stream()
     idx, _ = moe.route(x, wr, b, shape)
     n_touched = int(torch.unique(idx).numel())
     rows = T * shape.top_k
+    fp8 = experts_fp8 is not None
 
     def step():
-        moe.forward(x, wr, b, wg, wu, wd, shape, out=out, stream=stream)
+        if fp8:
+            moe.forward_fp8(x, wr, b, experts_fp8, shape, out=out, stream=stream)
+        else:
+            moe.forward(x, wr, b, wg, wu, wd, shape, out=out, stream=stream)
 
     for _ in range(warmup):
         flush.zero_()
@@ -193,7 +202,7 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     abi.beam_moe_timing_enable(False)
     stage_ms = {k: v / n2 for k, v in stage_sum.items()}
 
-    layer_flops, layer_bytes, kern = algorithmic(shape, T, n_touched, rows)
+    layer_flops, layer_bytes, kern = algorithmic(shape, T, n_touched, rows, fp8)
     t_roof_s = max(layer_flops / (pk["bf16_tflops"] * 1e12), layer_bytes / (pk["hbm_gbs"] * 1e9))
     ms_per_step = total_ms / steps
     dom = "expert_mlp"
@@ -208,7 +217,7 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     roof["kernel"] = dom
     roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
     roof["kernel_ms"] = stage_ms[dom]
-    tr = TRAFFIC.get(name)
+    tr = None if fp8 else TRAFFIC.get(name)
     roof["traffic"] = tr["bytes_per_touched_expert"] * n_touched if tr and tr.get("kernel") == dom else None
 
     res = {
@@ -305,6 +314,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-tokens", type=int, default=None)
     ap.add_argument("--n-group", type=int, default=8, help="expert groups of 32 (8 = Beam); fewer for profiling")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"], help="expert weights of the headline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -346,9 +356,12 @@ def main():
     experts = W.make_experts(shape, 0, device)
     torch.cuda.synchronize()
 
-    res = measure(name, shape, T, hot, args.steps, args.warmup, experts, device, flush, pk)
+    head_fp8 = W.make_experts_fp8(shape, 0, device) if args.weights == "fp8" else None
+    res = measure(name, shape, T, hot, args.steps, args.warmup, experts, device, flush, pk, e2e=head_fp8 is None,
+                  experts_fp8=head_fp8)
+    del head_fp8
     secondary = None
-    if not args.no_secondary and name == "decode" and args.n_group == 8:
+    if not args.no_secondary and name == "decode" and args.n_group == 8 and args.weights == "bf16":
         s_name, s_shape, s_T, s_hot = workload("prefill")
         s_steps = max(10, min(args.steps, 50))
         sec = measure(s_name, s_shape, s_T, s_hot, s_steps, args.warmup, experts, device, flush, pk, e2e=False)
@@ -356,6 +369,22 @@ def main():
                      "ms_per_step": sec["ms_per_step"], "steps": s_steps, "roofline": sec["roofline"],
                      "layer_roofline": sec["layer_roofline"], "stage_ms": sec["stage_ms"],
                      "n_touched_experts": sec["n_touched_experts"]}
+
+    fp8 = None
+    if not args.no_secondary and name == "decode" and args.n_group == 8 and args.weights == "bf16":
+        # The block on FP8 E4M3 expert weights (same draws, quantised per row): decode and prefill.
+        experts_fp8 = W.make_experts_fp8(shape, 0, device)
+        fp8 = {}
+        for f_name in ("decode", "prefill"):
+            f_name, f_shape, f_T, f_hot = workload(f_name)
+            f_steps = args.steps if f_name == "decode" else max(10, min(args.steps, 50))
+            r = measure(f_name, f_shape, f_T, f_hot, f_steps, args.warmup, experts, device, flush, pk, e2e=False,
+                        experts_fp8=experts_fp8)
+            fp8[f_name] = {"workload": f"Beam {f_name} T={f_T}, FP8 E4M3 experts (per-row FP32 scales)",
+                           "value": r["value"], "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
+                           "steps": f_steps, "roofline": r["roofline"], "layer_roofline": r["layer_roofline"],
+                           "stage_ms": r["stage_ms"], "clocks": r["clocks"]}
+        del experts_fp8
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -375,19 +404,22 @@ def main():
                        "T": T, "d": shape.d, "I": shape.I, "E": shape.E, "n_group": shape.n_group,
                        "topk_group": shape.topk_group, "top_k": shape.top_k, "scale": shape.scale,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "flushed (512 MB write) before every timed step"},
+                       "l2": "flushed (512 MB write) before every timed step",
+                       "expert_weights": "BF16" if args.weights == "bf16" else "FP8 E4M3, per-row FP32 scales"},
             "roofline": {**res["roofline"], "peak_source": pk_src + " (MEASURED_PEAKS.json burst)"
                          if pk_src == "measured" else "fallback"},
             "layer_roofline": res["layer_roofline"],
             "stage_ms": res["stage_ms"],
             "n_touched_experts": res["n_touched_experts"],
             "cpu_baseline": cpu,
-            "e2e": res["e2e"],
+            "e2e": res.get("e2e"),
             "gpu_launches": res["gpu_launches"],
             "clocks": res["clocks"],
         }
         if secondary:
             line["secondary"] = secondary
+        if fp8:
+            line["fp8_experts"] = fp8
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

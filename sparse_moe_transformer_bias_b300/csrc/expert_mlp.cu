@@ -41,11 +41,12 @@
 // leave their loops, copies and MMAs already issued are drained (bounded), and TMEM is
 // freed before the CTA exits.
 //
-// FP8 weights (kFP8): the weights are E4M3 codes with one FP32 scale per output row. TMA
-// streams the byte tiles [128 x 64] (64-byte swizzle) next to the BF16 token rows; eight
-// converter warps (two per TMEM lane quarter, one per weight tile of the stage) widen each
-// row's 64 codes and store them with tcgen05.st into a ring of A buffers in TMEM, and the
-// MMA reads A from TMEM (B, the token rows, still from shared memory). The widening is
+// FP8 weights (kFP8): the weights are E4M3 codes with one FP32 scale per output row. A
+// stage covers K = 128: TMA streams the byte tiles [128 x 128] (128-byte rows, 128-byte
+// swizzle; as many bytes per copy as a BF16 tile) and the token rows as two 64-wide BF16
+// halves; eight converter warps (two per TMEM lane quarter, one per weight tile of the
+// stage) widen each row's 128 codes and store them with tcgen05.st into a ring of A
+// buffers in TMEM, and the MMA reads A from TMEM (B, the token rows, from shared memory). The widening is
 // exact: E4M3 -> F16 by cvt (every finite code is an F16 normal or zero), then F16 -> BF16
 // by moving the exponent and mantissa bits down three places, which keeps every bit and
 // multiplies the value by 2^-112 (zero stays zero; every nonzero code lands on a BF16
@@ -67,15 +68,17 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 template <int kBNMax, bool kFP8>
 struct MlpCfg {
     static constexpr int kThreads = kThreadsFor(kFP8);
-    static constexpr int kA = kTileM * kTileK * (kFP8 ? 1 : 2);  // one weight tile in shared memory
-    static constexpr int kB = kBNMax * kTileK * 2;
+    static constexpr int kKStage = kFP8 ? 2 * kTileK : kTileK;  // K per stage
+    static constexpr int kA = kTileM * kKStage * (kFP8 ? 1 : 2);  // one weight tile in shared memory
+    static constexpr int kBHalf = kBNMax * kTileK * 2;          // token rows x 64 of K (one swizzle row)
+    static constexpr int kB = kBHalf * (kKStage / kTileK);
     static constexpr int kStage = 2 * kA + kB;
     static constexpr int kBudget = 227 * 1024 - 2048;
     static constexpr int kStages = (kBudget / kStage) > 10 ? 10 : (kBudget / kStage);
     // FP8: a ring of converted A buffers in TMEM, each the stage's two weight tiles as BF16
-    // (2 x 32 columns), after the accumulator slots.
-    static constexpr int kABufs = kFP8 ? 4 : 0;
-    static constexpr int kACols = 2 * kTileK / 2;
+    // (2 x 64 columns), after the accumulator slots.
+    static constexpr int kACols = kFP8 ? 2 * kKStage / 2 : 0;
+    static constexpr int kABufs = kFP8 ? (kBNMax <= 32 ? 3 : 2) : 0;
     static constexpr int kAccCols = 512 - kABufs * kACols;
     static constexpr int kSlots = (kAccCols / kBNMax) < 4 ? (kAccCols / kBNMax) : 4;
     static constexpr int kABase = kSlots * kBNMax;  // first TMEM column of the A buffers
@@ -278,12 +281,12 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                     fence_proxy_async_global();  // order the copies below after that observation
                 }
                 const int b_rows = ((it.tl.z + kBoxRows - 1) / kBoxRows) * kBoxRows;
-                const uint32_t bytes = 2 * C::kA + b_rows * kTileK * 2;
+                const uint32_t bytes = 2 * C::kA + b_rows * C::kKStage * 2;
                 const int k_chunks = it.down ? args.kc_dn : args.kc_gu;
                 const int a_row = it.down ? it.tl.x * args.d + it.m * 2 * kTileM : it.tl.x * args.I + it.m * kTileM;
                 const BMaps& bm = it.down ? tmH : tmX;
                 for (int kc = 0; kc < k_chunks; ++kc) {
-                    const int kx = kc * kTileK;
+                    const int kx = kc * C::kKStage;
                     if (!ptx::mbar_wait(bar(EMPTY0 + stage), phase ^ 1, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
@@ -300,11 +303,15 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                         ptx::tma_load_2d(sa + C::kA, &tmWu, kx, a_row, bar(FULL0 + stage), pol_w);
                     }
                     const uint32_t sb = sa + 2 * C::kA;
-                    for (int i = kBoxKinds - 1, r = 0; i >= 0; --i) {
-                        const int hh = kBoxRows << i;
-                        if (hh > kBNMax || b_rows - r < hh) continue;
-                        ptx::tma_load_2d(sb + r * kTileK * 2, &bm.m[i], kx, it.tl.y + r, bar(FULL0 + stage), pol_x);
-                        r += hh;
+#pragma unroll
+                    for (int half = 0; half < C::kKStage / kTileK; ++half) {
+                        for (int i = kBoxKinds - 1, r = 0; i >= 0; --i) {
+                            const int hh = kBoxRows << i;
+                            if (hh > kBNMax || b_rows - r < hh) continue;
+                            ptx::tma_load_2d(sb + half * C::kBHalf + r * kTileK * 2, &bm.m[i], kx + half * kTileK,
+                                             it.tl.y + r, bar(FULL0 + stage), pol_x);
+                            r += hh;
+                        }
                     }
                     issued |= 1u << stage;
                     parity = (parity & ~(1u << stage)) | (phase << stage);
@@ -367,13 +374,15 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                     const uint32_t sa = ptx::smem_u32(smem + stage * C::kStage);
                     const uint32_t sb = sa + 2 * C::kA;
 #pragma unroll
-                    for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
-                        const uint64_t bdesc = ptx::sw128_kmajor_desc(sb + kk * kMmaK * 2);
+                    for (int kk = 0; kk < C::kKStage / kMmaK; ++kk) {
+                        constexpr int kPerRow = kTileK / kMmaK;  // K steps per 128-byte swizzle row
+                        const uint64_t bdesc =
+                            ptx::sw128_kmajor_desc(sb + (kk / kPerRow) * C::kBHalf + (kk % kPerRow) * kMmaK * 2);
                         const uint32_t accum = (kc | kk) ? 1u : 0u;
                         if constexpr (kFP8) {
                             const uint32_t ta = tmem_base + C::kABase + abuf * C::kACols + kk * (kMmaK / 2);
                             ptx::mma_bf16_ta(d0, ta, bdesc, idesc, accum);
-                            ptx::mma_bf16_ta(d1, ta + kTileK / 2, bdesc, idesc, accum);
+                            ptx::mma_bf16_ta(d1, ta + C::kKStage / 2, bdesc, idesc, accum);
                         } else {
                             ptx::mma_bf16(d0, ptx::sw128_kmajor_desc(sa + kk * kMmaK * 2), bdesc, idesc, accum);
                             ptx::mma_bf16(d1, ptx::sw128_kmajor_desc(sa + C::kA + kk * kMmaK * 2), bdesc, idesc,
@@ -415,7 +424,7 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
             const int q = warp & 3;
             const int t = (warp - 2 - kEpiWarps) >> 2;
             const int r = q * 32 + lane;
-            const int swz = (r >> 1) & 3;  // the 64-byte swizzle of the byte tile
+            const int swz = r & 7;  // the 128-byte swizzle of the byte tile
             const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
             int stage = 0, rslot = 0, abuf = 0;
             uint32_t phase = 0, rphase = 0, aphase = 0;
@@ -443,19 +452,24 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint8_t* src = smem + stage * C::kStage + t * C::kA + r * kTileK;
-                    uint4 v[4];
+                    const uint8_t* src = smem + stage * C::kStage + t * C::kA + r * C::kKStage;
+                    const uint32_t dst = tmem_base + lane_off + C::kABase + abuf * C::kACols + t * (C::kKStage / 2);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(src + 16 * (j ^ swz));
-                    uint32_t o[32];
+                    for (int part = 0; part < C::kKStage / 64; ++part) {  // 64 codes -> 32 columns
+                        uint4 v[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        e4m3x4_to_bf16x4_scaled(v[j].x, o[8 * j + 0], o[8 * j + 1]);
-                        e4m3x4_to_bf16x4_scaled(v[j].y, o[8 * j + 2], o[8 * j + 3]);
-                        e4m3x4_to_bf16x4_scaled(v[j].z, o[8 * j + 4], o[8 * j + 5]);
-                        e4m3x4_to_bf16x4_scaled(v[j].w, o[8 * j + 6], o[8 * j + 7]);
+                        for (int j = 0; j < 4; ++j)
+                            v[j] = *reinterpret_cast<const uint4*>(src + 16 * ((4 * part + j) ^ swz));
+                        uint32_t o[32];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            e4m3x4_to_bf16x4_scaled(v[j].x, o[8 * j + 0], o[8 * j + 1]);
+                            e4m3x4_to_bf16x4_scaled(v[j].y, o[8 * j + 2], o[8 * j + 3]);
+                            e4m3x4_to_bf16x4_scaled(v[j].z, o[8 * j + 4], o[8 * j + 5]);
+                            e4m3x4_to_bf16x4_scaled(v[j].w, o[8 * j + 6], o[8 * j + 7]);
+                        }
+                        ptx::tmem_st32(dst + 32 * part, o);
                     }
-                    ptx::tmem_st32(tmem_base + lane_off + C::kABase + abuf * C::kACols + t * (kTileK / 2), o);
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
@@ -657,7 +671,7 @@ cudaError_t launch_dense_tiles(int T, int bn_max, int4* tiles, int* tile_done, c
 namespace {
 
 MlpArgs mlp_args(const Shape& s, int rows, const int4* tiles, int* tile_done, int max_tiles, bf16* h, bf16* y,
-                 int* status) {
+                 int* status, int k_stage) {
     MlpArgs a;
     a.tiles = tiles;
     a.next_item = const_cast<int*>(reinterpret_cast<const int*>(tiles)) + 1;
@@ -667,8 +681,8 @@ MlpArgs mlp_args(const Shape& s, int rows, const int4* tiles, int* tile_done, in
     a.rows = rows;
     a.m_gu = s.I / kTileM;
     a.m_dn = (s.d / kTileM + 1) / 2;
-    a.kc_gu = s.d / kTileK;
-    a.kc_dn = s.I / kTileK;
+    a.kc_gu = s.d / k_stage;
+    a.kc_dn = s.I / k_stage;
     a.I = s.I;
     a.d = s.d;
     a.h = h;
@@ -697,7 +711,7 @@ cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_
         !encode_tmap_bf16_2d(&wd, w_down, static_cast<uint64_t>(s.E) * s.d, s.I, kTileM, kTileK, &why) ||
         !encode_bmaps(&bx, x_perm, rows, s.d, bn_max, &why) || !encode_bmaps(&bh, h, rows, s.I, bn_max, &why))
         return cudaErrorInvalidValue;
-    const MlpArgs a = mlp_args(s, rows, tiles, tile_done, max_tiles, h, y, status);
+    const MlpArgs a = mlp_args(s, rows, tiles, tile_done, max_tiles, h, y, status, kTileK);
     const int grid = mlp_grid(a, max_tiles, num_sms);
     if (bn_max <= 32) return launch_mlp<32, false>(wg, wu, wd, bx, bh, a, grid, st);
     if (bn_max <= 128) return launch_mlp<128, false>(wg, wu, wd, bx, bh, a, grid, st);
@@ -711,12 +725,13 @@ cudaError_t launch_expert_mlp_fp8(const Shape& s, const Fp8Experts& q, const bf1
     CUtensorMap wg, wu, wd;
     BMaps bx, bh;
     const char* why = nullptr;
-    if (!encode_tmap_u8_2d(&wg, q.wg, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kTileK, &why) ||
-        !encode_tmap_u8_2d(&wu, q.wu, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kTileK, &why) ||
-        !encode_tmap_u8_2d(&wd, q.wd, static_cast<uint64_t>(s.E) * s.d, s.I, kTileM, kTileK, &why) ||
+    constexpr int kKStage = 2 * kTileK;  // FP8 stages: 128 codes of K (128-byte rows)
+    if (!encode_tmap_u8_2d(&wg, q.wg, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kKStage, &why) ||
+        !encode_tmap_u8_2d(&wu, q.wu, static_cast<uint64_t>(s.E) * s.I, s.d, kTileM, kKStage, &why) ||
+        !encode_tmap_u8_2d(&wd, q.wd, static_cast<uint64_t>(s.E) * s.d, s.I, kTileM, kKStage, &why) ||
         !encode_bmaps(&bx, x_perm, rows, s.d, bn_max, &why) || !encode_bmaps(&bh, h, rows, s.I, bn_max, &why))
         return cudaErrorInvalidValue;
-    MlpArgs a = mlp_args(s, rows, tiles, tile_done, max_tiles, h, y, status);
+    MlpArgs a = mlp_args(s, rows, tiles, tile_done, max_tiles, h, y, status, kKStage);
     a.gs = q.gs;
     a.us = q.us;
     a.ds = q.ds;

@@ -171,8 +171,8 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint
                          uint32_t box_cols, const char** why);
 
 // Host helper: encode a 2-D byte tensor map (FP8 codes, rows x cols, row-major) with the
-// 64-byte swizzle: in shared memory the 16-byte chunk c of row r of a 64-byte-wide box sits
-// at chunk c ^ ((r >> 1) & 3).
+// 128-byte swizzle (box_cols <= 128): in shared memory the 16-byte chunk c of row r of a
+// 128-byte-wide box sits at chunk c ^ (r & 7).
 bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                        uint32_t box_cols, const char** why);
 

@@ -1,6 +1,6 @@
 // Host helpers for the TMA tensor maps of the tcgen05 kernels (router_gemm.cu,
-// expert_mlp.cu): BF16 row-major matrices with the 128-byte swizzle, and FP8 (byte)
-// matrices with the 64-byte swizzle, boxes of 64 columns.
+// expert_mlp.cu): BF16 row-major matrices (boxes of 64 columns) and FP8 byte matrices
+// (boxes of 128 columns), both with the 128-byte swizzle.
 #include <mutex>
 
 #include "internal.cuh"
@@ -62,7 +62,7 @@ bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *why = "cuTensorMapEncodeTiled rejected a tensor map";
