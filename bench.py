@@ -42,11 +42,16 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM bytes (read + write) per launch of the dominant kernel from ncu captures; remove an
-# entry when its kernel changes after the capture. Keys: workload name.
-# decode: an `ncu --set full` capture of the expert kernel on 32 experts read 2.517993 GB
-# and wrote 4.866 MB (per touched expert: 78.69 MB + 0.152 MB); a full launch moves that
-# per touched expert.
-TRAFFIC = {"decode": {"kernel": "expert_mlp", "bytes_per_touched_expert": (2.517993e9 + 4.866304e6) / 32}}
+# entry when its kernel changes after the capture. Keys: workload name. Each capture ran the
+# same kernel instance on one group of 32 experts (a full-size process holds more than a
+# capture may): its traffic per touched expert times the experts a full launch touches.
+# decode (BF16): 2.518033 GB read, 4.626 MB written for 32 experts (78.69 MB per expert: the
+# weights once). prefill: the T=512 case on 32 experts (about 128 rows per expert, as at
+# T=4096 on 256): 2.679522 GB read, 21.94 MB written. decode (FP8): 1.261035 GB read,
+# 3.992 MB written for 32 experts.
+TRAFFIC = {"decode": {"kernel": "expert_mlp", "bytes_per_touched_expert": (2.518033e9 + 4.625920e6) / 32},
+           "prefill": {"kernel": "expert_mlp", "bytes_per_touched_expert": (2.679522e9 + 21.939968e6) / 32}}
+TRAFFIC_FP8 = {"decode": {"kernel": "expert_mlp", "bytes_per_touched_expert": (1.261035e9 + 3.992064e6) / 32}}
 
 
 def peaks():
@@ -217,7 +222,7 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     roof["kernel"] = dom
     roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
     roof["kernel_ms"] = stage_ms[dom]
-    tr = None if fp8 else TRAFFIC.get(name)
+    tr = (TRAFFIC_FP8 if fp8 else TRAFFIC).get(name)
     roof["traffic"] = tr["bytes_per_touched_expert"] * n_touched if tr and tr.get("kernel") == dom else None
 
     res = {

@@ -78,6 +78,29 @@ def test_every_finite_code_is_widened_exactly():
     run_and_check(shape, x, wr, b, q8, np.arange(T), "all codes")
 
 
+def test_subnormal_codes_only():
+    """Weights made of the 16 codes with exponent field 0 (zeros and subnormals, both signs),
+    scaled so that the outputs are O(1): a path that flushed subnormal weights, or their
+    products, would lose the whole signal and fail the relative error bound."""
+    shape = W.TINY
+    E, d, I = shape.E, shape.d, shape.I
+    pool = torch.tensor([s | m for s in (0, 0x80) for m in range(8)], dtype=torch.uint8)
+    gen = torch.Generator().manual_seed(5)
+
+    def codes(rows, cols):
+        return pool[torch.randint(0, len(pool), (E, rows, cols), generator=gen)].cuda()
+
+    def scales(rows, fan_in):
+        return torch.full((E, rows), 1.0 / (0.007 * fan_in ** 0.5), device="cuda")
+
+    q8 = ((codes(I, d), scales(I, d)), (codes(I, d), scales(I, d)), (codes(d, I), scales(d, I)))
+    T = 48
+    x = W.make_tokens(shape, T, 6, "cuda")
+    wr, b = W.make_router(shape, 6, "cuda")
+    out = run_and_check(shape, x, wr, b, q8, np.arange(T), "subnormal codes")
+    assert np.abs(out).max() > 0.05
+
+
 def test_fp8_deterministic(tiny_fp8):
     shape = W.TINY
     x = W.make_tokens(shape, 300, 7, "cuda")
