@@ -107,11 +107,13 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int nchunks, int E,
         }
         for (int c = 0; c < nchunks; ++c) chunk_count[static_cast<size_t>(c) * E + e] += base;
         if (nt > 0) {
-            int tile = ntl[e] - nt;
-            for (int r = 0; r < n; r += per) {
+            const int first = ntl[e] - nt;
+            for (int r = 0, tile = first; r < n; r += per, ++tile) {
                 const int rows = min(per, n - r);
                 if (tile_done) tile_done[tile] = 0;
-                tiles[1 + tile++] = make_int4(e, base + r, rows, 0);
+                // .w: the tile's index among its expert's tiles and their count (the
+                // expert kernel orders its items m-major within an expert)
+                tiles[1 + tile] = make_int4(e, base + r, rows, (tile - first) | (nt << 16));
             }
         }
     }

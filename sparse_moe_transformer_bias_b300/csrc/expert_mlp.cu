@@ -17,7 +17,12 @@
 // Item ids run over every gate/up item, then every down item; CTAs take the next id from
 // an atomic counter (dynamic scheduling), so no SM idles while work is left and the down
 // items start on SMs that finish gate/up work early, with no kernel boundary between the
-// two products. A down item of tile n reads h rows that the gate/up items of tile n write:
+// two products. Within one expert the ids run m-major over the expert's N-tiles (the items
+// of weight tile m for every N-tile of the expert, then m + 1, ...): an expert with more
+// rows than one N-tile holds has its N-tiles' items of the same weight tile handed out
+// together, so the CTAs running them stream those weights at the same time and the
+// repeats are served by L2 instead of HBM (those weight loads carry the normal L2
+// priority; weights read once carry evict-first). A down item of tile n reads h rows that the gate/up items of tile n write:
 // each epilogue warp of a gate/up item increments tile_done[n] after its stores, and the
 // producer of a down item waits (bounded) until tile_done[n] counts every warp of every
 // gate/up item of the tile. All gate/up ids are handed out before any down id, and a
@@ -99,7 +104,8 @@ struct MlpCfg {
 };
 
 struct MlpArgs {
-    const int4* tiles;   // header int4 {tile count, next item id, 0, 0}, then {e, row0, rows, 0}
+    const int4* tiles;   // header int4 {tile count, next item id, 0, 0}, then per N-tile
+                         // {e, row0, rows, index among the expert's tiles | their count << 16}
     int* next_item;      // = &tiles[0].y, zeroed by dispatch for every call
     int* tile_done;      // [max_tiles] gate/up items finished per tile, zeroed by dispatch
     int max_tiles;
@@ -120,20 +126,35 @@ struct MItem {
     int4 tl;     // {expert, first row, rows, 0}
     int tile;
     int m;
+    int n_t;     // N-tiles of the item's expert
     bool down;
     bool ok;
 };
 
-__device__ __forceinline__ MItem decode(const MlpArgs& a, int id, int n_gu) {
+// Item id -> (N-tile, weight tile m). The ids of one expert's n_t consecutive N-tiles
+// (first .. first + n_t - 1) are [first * mt, (first + n_t) * mt), taken m-major.
+__device__ __forceinline__ MItem decode(const MlpArgs& a, int id, int n_gu, int n_tiles) {
     MItem it;
     it.down = id >= n_gu;
     const int j = it.down ? id - n_gu : id;
     const int mt = it.down ? a.m_dn : a.m_gu;
-    it.tile = j / mt;
-    it.m = j % mt;
+    const int tg = j / mt;  // a tile of the right expert
+    const int w = a.tiles[1 + tg].w;
+    const int t_in = w & 0xffff, n_t = (w >> 16) & 0xffff;
+    const int first = tg - t_in;
+    bool ok = n_t >= 1 && t_in < n_t && first >= 0 && first + n_t <= n_tiles;
+    it.n_t = n_t;
+    if (ok) {
+        const int local = j - first * mt;
+        it.m = local / n_t;
+        it.tile = first + local % n_t;
+    } else {
+        it.m = 0;
+        it.tile = tg;
+    }
     const int4 tl = a.tiles[1 + it.tile];
     it.tl = tl;
-    it.ok = !(tl.x < 0 || tl.x >= a.n_experts || tl.z <= 0 || tl.z > 256 || tl.y < 0 || tl.y > a.rows - tl.z);
+    it.ok = ok && !(tl.x < 0 || tl.x >= a.n_experts || tl.z <= 0 || tl.z > 256 || tl.y < 0 || tl.y > a.rows - tl.z);
     return it;
 }
 
@@ -246,7 +267,11 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------ scheduler + TMA producer
-            const uint64_t pol_w = ptx::policy_evict_first();
+            // Weights of an expert with one N-tile are read once: evict first. An expert
+            // with several N-tiles has its weight tiles streamed by several CTAs at about
+            // the same time (m-major ids): normal priority, so that the others hit L2.
+            const uint64_t pol_w_once = ptx::policy_evict_first();
+            const uint64_t pol_w_shared = ptx::policy_evict_normal();
             const uint64_t pol_x = ptx::policy_evict_last();
             int stage = 0, rslot = 0;
             uint32_t phase = 0, rphase = 0;
@@ -267,7 +292,7 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                     rphase ^= 1;
                 }
                 if (id < 0) break;
-                const MItem it = decode(args, id, n_gu);
+                const MItem it = decode(args, id, n_gu, n_tiles);
                 if (!it.ok || it.tl.z > kBNMax) {
                     flag_status(status, kStatusBadIndex);
                     continue;
@@ -285,6 +310,7 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                 const int k_chunks = it.down ? args.kc_dn : args.kc_gu;
                 const int a_row = it.down ? it.tl.x * args.d + it.m * 2 * kTileM : it.tl.x * args.I + it.m * kTileM;
                 const BMaps& bm = it.down ? tmH : tmX;
+                const uint64_t pol_w = it.n_t > 1 ? pol_w_shared : pol_w_once;
                 for (int kc = 0; kc < k_chunks; ++kc) {
                     const int kx = kc * C::kKStage;
                     if (!ptx::mbar_wait(bar(EMPTY0 + stage), phase ^ 1, abort_flag, kWaitLimitNs)) {
@@ -347,7 +373,7 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                     rphase ^= 1;
                 }
                 if (id < 0) break;
-                const MItem it = decode(args, id, n_gu);
+                const MItem it = decode(args, id, n_gu, n_tiles);
                 if (!it.ok || it.tl.z > kBNMax) continue;
                 const int s0 = slot, s1 = (slot + 1) % C::kSlots;
                 if (!ptx::mbar_wait(bar(TEMPTY0 + s0), ((tph >> s0) & 1u) ^ 1u, abort_flag, kWaitLimitNs) ||
@@ -442,7 +468,7 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                     rphase ^= 1;
                 }
                 if (id < 0) break;
-                const MItem it = decode(args, id, n_gu);
+                const MItem it = decode(args, id, n_gu, n_tiles);
                 if (!it.ok || it.tl.z > kBNMax) continue;
                 const int k_chunks = it.down ? args.kc_dn : args.kc_gu;
                 for (int kc = 0; kc < k_chunks; ++kc) {
@@ -514,7 +540,7 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                 rphase ^= 1;
             }
             if (id < 0) break;
-            const MItem it = decode(args, id, n_gu);
+            const MItem it = decode(args, id, n_gu, n_tiles);
             if (!it.ok || it.tl.z > kBNMax) continue;
             const int s0 = slot, s1 = (slot + 1) % C::kSlots;
             if (!ptx::mbar_wait(bar(TFULL0 + s0), (tph >> s0) & 1u, abort_flag, kWaitLimitNs) ||
@@ -652,7 +678,7 @@ __global__ void __launch_bounds__(256) dense_tiles_kernel(int T, int bn_max, int
     const int per = min(bn_max, (((T + q - 1) / q + 15) / 16) * 16);
     const int nt = (T + per - 1) / per;
     for (int i = threadIdx.x; i < nt; i += blockDim.x) {
-        tiles[1 + i] = make_int4(0, i * per, min(per, T - i * per), 0);
+        tiles[1 + i] = make_int4(0, i * per, min(per, T - i * per), i | (nt << 16));
         tile_done[i] = 0;
     }
     if (threadIdx.x == 0) tiles[0] = make_int4(nt, 0, 0, 0);
