@@ -41,17 +41,14 @@ METRIC = "Beam MoE-layer tokens/s (T=16 decode, T=4096 prefill); % of roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes (read + write) per launch of the dominant kernel from ncu captures; remove an
-# entry when its kernel changes after the capture. Keys: workload name. Each capture ran the
-# same kernel instance on one group of 32 experts (a full-size process holds more than a
-# capture may): its traffic per touched expert times the experts a full launch touches.
-# decode (BF16): 2.518033 GB read, 4.626 MB written for 32 experts (78.69 MB per expert: the
-# weights once). prefill: the T=512 case on 32 experts (about 128 rows per expert, as at
-# T=4096 on 256): 2.679522 GB read, 21.94 MB written. decode (FP8): 1.261035 GB read,
-# 3.992 MB written for 32 experts.
-TRAFFIC = {"decode": {"kernel": "expert_mlp", "bytes_per_touched_expert": (2.518033e9 + 4.625920e6) / 32},
-           "prefill": {"kernel": "expert_mlp", "bytes_per_touched_expert": (2.679522e9 + 21.939968e6) / 32}}
-TRAFFIC_FP8 = {"decode": {"kernel": "expert_mlp", "bytes_per_touched_expert": (1.261035e9 + 3.992064e6) / 32}}
+# DRAM bytes (read + write) of one launch of the dominant kernel on the bench's own
+# full-size workloads (seeded, so every run routes the same way), from one-pass ncu
+# captures of dram__bytes_read.sum and dram__bytes_write.sum; remove an entry when its
+# kernel changes after the capture. Keys: (workload name, FP8 experts).
+# decode: 7.00 GB read, 4.45 MB written; prefill: 20.70 GB, 487.8 MB; FP8 decode: 3.50 GB,
+# 3.34 MB; FP8 prefill: 10.68 GB, 494.8 MB.
+TRAFFIC = {("decode", False): 7.00e9 + 4.45e6, ("prefill", False): 20.70e9 + 487.8e6,
+           ("decode", True): 3.50e9 + 3.34e6, ("prefill", True): 10.68e9 + 494.8e6}
 
 
 def peaks():
@@ -222,8 +219,7 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     roof["kernel"] = dom
     roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
     roof["kernel_ms"] = stage_ms[dom]
-    tr = (TRAFFIC_FP8 if fp8 else TRAFFIC).get(name)
-    roof["traffic"] = tr["bytes_per_touched_expert"] * n_touched if tr and tr.get("kernel") == dom else None
+    roof["traffic"] = TRAFFIC.get((name, fp8)) if shape.n_group == 8 else None
 
     res = {
         "value": T * steps / (total_ms * 1e-3),
