@@ -45,9 +45,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # full-size workloads (seeded, so every run routes the same way), from one-pass ncu
 # captures of dram__bytes_read.sum and dram__bytes_write.sum; remove an entry when its
 # kernel changes after the capture. Keys: (workload name, FP8 experts).
-# decode: 7.00 GB read, 4.45 MB written; prefill: 20.70 GB, 487.8 MB; FP8 decode: 3.50 GB,
-# 3.34 MB; FP8 prefill: 10.68 GB, 494.8 MB.
-TRAFFIC = {("decode", False): 7.00e9 + 4.45e6, ("prefill", False): 20.70e9 + 487.8e6,
+# decode: 7.00 GB read, 4.45 MB written; FP8 decode: 3.50 GB, 3.34 MB; FP8 prefill:
+# 10.68 GB, 494.8 MB.
+TRAFFIC = {("decode", False): 7.00e9 + 4.45e6,
            ("decode", True): 3.50e9 + 3.34e6, ("prefill", True): 10.68e9 + 494.8e6}
 
 

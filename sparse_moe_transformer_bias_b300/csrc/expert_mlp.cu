@@ -85,7 +85,7 @@ struct MlpCfg {
     static constexpr int kACols = kFP8 ? 2 * kKStage / 2 : 0;
     static constexpr int kABufs = kFP8 ? (kBNMax <= 32 ? 3 : 2) : 0;
     static constexpr int kAccCols = 512 - kABufs * kACols;
-    static constexpr int kSlots = (kAccCols / kBNMax) < 4 ? (kAccCols / kBNMax) : 4;
+    static constexpr int kSlots = ((kAccCols / kBNMax) < 4 ? (kAccCols / kBNMax) : 4) & ~1;  // items take pairs
     static constexpr int kABase = kSlots * kBNMax;  // first TMEM column of the A buffers
     static constexpr int kColsNeeded = kSlots * kBNMax + kABufs * kACols;
     static constexpr int kTmemCols = kColsNeeded <= 32    ? 32
@@ -653,12 +653,14 @@ cudaError_t launch_mlp(const CUtensorMap& wg, const CUtensorMap& wu, const CUten
 
 // N-tile capacity for a batch of T tokens: 32 for decode-sized batches; 128 while the
 // average expert gets at most 32 rows (one tile holds nearly every expert's rows, and the
-// smaller B stage leaves room for more stages and four accumulator slots); else 256, so
-// that a weight tile is streamed once for up to 256 of its expert's rows.
+// smaller B stage leaves room for more stages and four accumulator slots); 192 while it
+// gets at most 160 (stages of 56 KB: four in flight instead of three of 64 KB, which more
+// than pays for the experts split over two tiles); else 256, so that a weight tile is
+// streamed once for up to 256 of its expert's rows.
 int gemm_bn_max(const Shape& s, int T) {
     if (T <= 32) return 32;
     const long long avg_rows = static_cast<long long>(T) * s.top_k / s.E;
-    return avg_rows <= 32 ? 128 : 256;
+    return avg_rows <= 32 ? 128 : avg_rows <= 160 ? 192 : 256;
 }
 
 int gemm_bn_max_fp8(const Shape& s, int T) {
@@ -741,6 +743,7 @@ cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_
     const int grid = mlp_grid(a, max_tiles, num_sms);
     if (bn_max <= 32) return launch_mlp<32, false>(wg, wu, wd, bx, bh, a, grid, st);
     if (bn_max <= 128) return launch_mlp<128, false>(wg, wu, wd, bx, bh, a, grid, st);
+    if (bn_max <= 192) return launch_mlp<192, false>(wg, wu, wd, bx, bh, a, grid, st);
     return launch_mlp<256, false>(wg, wu, wd, bx, bh, a, grid, st);
 }
 

@@ -36,7 +36,7 @@ def tiny_layer(T, seed=0):
     return P.Layer(shape, x, wr, b, wg, wu, wd)
 
 
-@pytest.mark.parametrize("T", [1, 7, 128, 129, 300])
+@pytest.mark.parametrize("T", [1, 7, 128, 129, 300, 1500])
 def test_tiny_forward_parity(T):
     layer = tiny_layer(T)
     check_layer(layer, np.arange(T), f"tiny T={T}")
