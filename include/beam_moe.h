@@ -227,7 +227,8 @@ BEAM_MOE_API int beam_moe_device_status(cudaStream_t stream);
  * (stage order: pre-norm, router weight split, router logits, router select, dispatch count,
  * dispatch scan, dispatch scatter, gather, expert MLP (gate/up, SwiGLU and down in one
  * kernel), combine (fused with the post-norm and residual in beam_moe_sublayer_forward);
- * unrun stages read 0). Returns the number of stages, or a negative error. */
+ * for T <= 128 the whole dispatch and gather is one launch, timed as dispatch count; unrun
+ * stages read 0). Returns the number of stages, or a negative error. */
 BEAM_MOE_API int beam_moe_timing_enable(int enable);
 BEAM_MOE_API int beam_moe_timing_read(float *ms, int max_stages);
 

@@ -307,12 +307,20 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
         LAUNCH(kSelect, launch_router_select(s, sc.partial, plan.splits, mode == 1 ? nullptr : bias, T, idx, w,
                                              mode == 1 ? logits : nullptr, st));
         if (fwd) {
-            LAUNCH(kCount, launch_dispatch_count(s, e_lo, se.E, idx, T, sc.chunk, dev->status, st));
-            LAUNCH(kScan, launch_dispatch_scan(se.E, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, sc.tile_done, st));
-            LAUNCH(kScatter, launch_dispatch_scatter(s, e_lo, se.E, idx, T, sc.chunk, sc.perm_src, sc.inv_slot,
-                                                     dev->status, st));
-            LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
-                                               dev->status, dev->num_sms, st));
+            if (T <= kSmallDispatchT) {
+                // one launch for the whole dispatch (timed as the count stage)
+                LAUNCH(kCount, launch_dispatch_small(s, e_lo, se.E, idx, T, bn_max, x, sc.expert_offset, sc.tiles,
+                                                     sc.tile_done, sc.perm_src, sc.inv_slot, sc.x_perm, dev->status,
+                                                     dev->num_sms, st));
+            } else {
+                LAUNCH(kCount, launch_dispatch_count(s, e_lo, se.E, idx, T, sc.chunk, dev->status, st));
+                LAUNCH(kScan,
+                       launch_dispatch_scan(se.E, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, sc.tile_done, st));
+                LAUNCH(kScatter, launch_dispatch_scatter(s, e_lo, se.E, idx, T, sc.chunk, sc.perm_src, sc.inv_slot,
+                                                         dev->status, st));
+                LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
+                                                   dev->status, dev->num_sms, st));
+            }
             if (mode == 5)
                 LAUNCH(kExpert, launch_expert_mlp_fp8(se, *q8, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
                                                       bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));

@@ -13,6 +13,10 @@
 //   scatter: permuted row of (t, k) = chunk base of e + rank; writes perm_src[row] = t
 //            and inv_slot[t, k] = row;
 //   gather:  x_perm[row] = x[perm_src[row]] with 16-byte loads and stores.
+// Small batches (T <= kSmallDispatchT, decode) run all four steps in one launch: every
+// block builds the same permutation in shared memory (per-expert token bitmaps of at most
+// four words), block 0 writes the work list, offsets, perm_src and inv_slot, and all
+// blocks copy their share of the rows. The result is the one the four kernels give.
 #include "internal.cuh"
 
 namespace beam {
@@ -172,6 +176,98 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     }
 }
 
+constexpr int kSmallWords = kSmallDispatchT / 32;
+constexpr int kSmallThreads = 256;  // >= the largest expert count (256)
+
+__global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
+    const int32_t* __restrict__ idx, int T, int E_all, int e_lo, int E, int K, int bn_max, const uint4* __restrict__ x,
+    int row_vecs, int* __restrict__ expert_offset, int4* __restrict__ tiles, int* __restrict__ tile_done,
+    int* __restrict__ perm_src, int* __restrict__ inv_slot, uint4* __restrict__ x_perm, int* status) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ uint32_t bm[kSmallThreads * kSmallWords];
+    __shared__ int base_s[kSmallThreads + 1];  // exclusive scan of rows per expert
+    __shared__ int tile_s[kSmallThreads + 1];  // exclusive scan of N-tiles per expert
+    __shared__ int src_s[kSmallDispatchT * 32];  // permuted row -> token
+    const int tid = threadIdx.x;
+    for (int i = tid; i < E * kSmallWords; i += blockDim.x) bm[i] = 0u;
+    __syncthreads();
+    const bool lead = blockIdx.x == 0;
+    for (int p = tid; p < T * K; p += blockDim.x) {
+        const int e = idx[p];
+        const int t = p / K;
+        if (e < 0 || e >= E_all) {
+            if (lead) atomicCAS(status, 0, kStatusBadExpert);
+            continue;
+        }
+        const int el = e - e_lo;
+        if (el >= 0 && el < E) atomicOr(&bm[el * kSmallWords + (t >> 5)], 1u << (t & 31));
+    }
+    __syncthreads();
+    // rows and N-tiles of expert tid (same split as dispatch_scan_kernel)
+    int n = 0, per = 0, nt = 0;
+    if (tid < E) {
+#pragma unroll
+        for (int w = 0; w < kSmallWords; ++w) n += __popc(bm[tid * kSmallWords + w]);
+        if (n > 0) {
+            const int q = (n + bn_max - 1) / bn_max;
+            per = min(bn_max, (((n + q - 1) / q + 15) / 16) * 16);
+            nt = (n + per - 1) / per;
+        }
+    }
+    base_s[tid + 1] = n;
+    tile_s[tid + 1] = nt;
+    if (tid == 0) base_s[0] = tile_s[0] = 0;
+    __syncthreads();
+    for (int off = 1; off < kSmallThreads; off <<= 1) {  // inclusive scans of entries 1..256
+        const int a = tid >= off ? base_s[tid + 1 - off] : 0;
+        const int b = tid >= off ? tile_s[tid + 1 - off] : 0;
+        __syncthreads();
+        base_s[tid + 1] += a;
+        tile_s[tid + 1] += b;
+        __syncthreads();
+    }
+    const int total_rows = base_s[E], total_tiles = tile_s[E];
+    if (lead && tid < E) {
+        const int base = base_s[tid], first = tile_s[tid];
+        expert_offset[tid] = base;
+        for (int r = 0, tile = first; r < n; r += per, ++tile) {
+            tile_done[tile] = 0;
+            tiles[1 + tile] = make_int4(tid, base + r, min(per, n - r), (tile - first) | (nt << 16));
+        }
+        if (tid == E - 1) {
+            expert_offset[E] = total_rows;
+            tiles[0] = make_int4(total_tiles, 0, 0, 0);
+        }
+    }
+    // row of every pair: expert base + the token's rank among the expert's tokens
+    for (int p = tid; p < T * K; p += blockDim.x) {
+        const int t = p / K;
+        const int el = idx[p] - e_lo;
+        if (el < 0 || el >= E || idx[p] < 0 || idx[p] >= E_all) {
+            if (lead) inv_slot[p] = -1;
+            continue;
+        }
+        int rank = __popc(bm[el * kSmallWords + (t >> 5)] & ((1u << (t & 31)) - 1u));
+        for (int w = 0; w < (t >> 5); ++w) rank += __popc(bm[el * kSmallWords + w]);
+        const int row = base_s[el] + rank;
+        src_s[row] = t;
+        if (lead) {
+            inv_slot[p] = row;
+            perm_src[row] = t;
+        }
+    }
+    __syncthreads();
+    // gather: this block's share of the 16-byte pieces of the dispatched rows
+    const long long total = static_cast<long long>(total_rows) * row_vecs;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + tid; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i / row_vecs);
+        const int v = static_cast<int>(i - static_cast<long long>(r) * row_vecs);
+        x_perm[i] = x[static_cast<size_t>(src_s[r]) * row_vecs + v];
+    }
+}
+
 }  // namespace
 
 int dispatch_max_tiles(const Shape& s, int T, int bn_max) {
@@ -203,6 +299,23 @@ cudaError_t launch_dispatch_scatter(const Shape& s, int e_lo, int E_loc, const i
     const size_t smem = static_cast<size_t>(E_loc) * kWords * sizeof(uint32_t);
     const cudaError_t le_ = launch_pdl(dispatch_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, st, topk_idx, T, s.E, e_lo, E_loc, s.top_k, chunk_base, perm_src,
                                                            inv_slot, status);
+    if (le_ != cudaSuccess) return le_;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_small(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T, int bn_max,
+                                  const bf16* x, int* expert_offset, int4* tiles, int* tile_done, int* perm_src,
+                                  int* inv_slot, bf16* x_perm, int* status, int num_sms, cudaStream_t st) {
+    if (T > kSmallDispatchT || E_loc > kSmallThreads || s.top_k > 32) return cudaErrorInvalidValue;
+    const int row_vecs = s.d / 8;
+    const long long total = static_cast<long long>(T) * s.top_k * row_vecs;
+    long long blocks = (total + 4 * kSmallThreads - 1) / (4 * kSmallThreads);
+    if (blocks > num_sms) blocks = num_sms;
+    if (blocks < 1) blocks = 1;
+    const cudaError_t le_ = launch_pdl(dispatch_small_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kSmallThreads),
+                                       0, st, topk_idx, T, s.E, e_lo, E_loc, s.top_k, bn_max,
+                                       reinterpret_cast<const uint4*>(x), row_vecs, expert_offset, tiles, tile_done,
+                                       perm_src, inv_slot, reinterpret_cast<uint4*>(x_perm), status);
     if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }

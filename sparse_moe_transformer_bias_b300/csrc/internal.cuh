@@ -80,6 +80,12 @@ cudaError_t launch_dispatch_scan(int E_loc, int T, int bn_max, int* chunk_count,
                                  int* tile_done, cudaStream_t st);
 cudaError_t launch_dispatch_scatter(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T,
                                     const int* chunk_base, int* perm_src, int* inv_slot, int* status, cudaStream_t st);
+// Count, scan, scatter and gather in one launch for small batches (T <= kSmallDispatchT,
+// E_loc <= 256, top_k <= 32): the same outputs as the four launches.
+constexpr int kSmallDispatchT = 128;
+cudaError_t launch_dispatch_small(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T, int bn_max,
+                                  const bf16* x, int* expert_offset, int4* tiles, int* tile_done, int* perm_src,
+                                  int* inv_slot, bf16* x_perm, int* status, int num_sms, cudaStream_t st);
 // x_perm[row] = x[perm_src[row]] for the *n_rows rows dispatched (rows: an upper bound).
 cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, const int* n_rows, int rows,
                                bf16* x_perm, int* status, int num_sms, cudaStream_t st);

@@ -4,7 +4,7 @@
 //
 // Stage 1: FP32 logits l = x . Wr^T (x is exactly BF16).
 //   T <= 32 (decode): router_logits_small_kernel on CUDA cores, FP32 fused multiply-adds,
-//   one CTA per two experts over the whole K, reduced in a fixed order.
+//   one CTA per expert over the whole K, reduced in a fixed order.
 //   T > 32: the tensor-core product of router_gemm.cu, after
 //   router_split_weights_kernel has written Wr as three BF16 pieces hi + mid + lo == Wr
 //   (exactly); the products x.piece are exact and accumulate in FP32. Split-K partial
@@ -29,7 +29,7 @@ constexpr unsigned kFull = 0xffffffffu;
 // FMA-ing in ascending K. The 32 lanes are combined by a fixed butterfly and the 8 warps
 // in warp order, so the result is deterministic.
 constexpr int kSmallT = 32;
-constexpr int kSmallEPB = 2;
+constexpr int kSmallEPB = 1;  // one CTA per expert: 256 CTAs, shorter per-lane token chains
 constexpr int kSmallWarps = 8;
 constexpr int kSmallMaxIt = 8;  // 128-wide K steps per warp: d <= 8 * 128 * 8
 

@@ -123,7 +123,20 @@ def test_launch_count_and_stage_timing():
         abi.beam_moe_timing_enable(False)
     ran = {k for k, v in times.items() if v > 0}
     assert n == len(ran), (n, times)
-    assert set(abi.STAGES) - ran <= {"pre_norm"}, times   # the plain forward has no pre-norm
+    # the plain forward has no pre-norm; for T <= 128 one launch covers the whole dispatch
+    assert set(abi.STAGES) - ran <= {"pre_norm", "dispatch_scan", "dispatch_scatter", "gather"}, times
+    assert {"router_logits", "router_select", "dispatch_count", "expert_mlp", "combine"} <= ran, times
+
+
+def test_large_batch_runs_every_dispatch_stage():
+    layer = tiny_layer(300)
+    abi.beam_moe_timing_enable(True)
+    try:
+        moe.forward(layer.x, layer.wr, layer.b, layer.wg, layer.wu, layer.wd, layer.shape)
+        times = abi.beam_moe_timing_read()
+    finally:
+        abi.beam_moe_timing_enable(False)
+    assert {"dispatch_count", "dispatch_scan", "dispatch_scatter", "gather"} <= {k for k, v in times.items() if v > 0}
 
 
 def test_host_buffers_end_to_end():
