@@ -45,10 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # full-size workloads (seeded, so every run routes the same way), from one-pass ncu
 # captures of dram__bytes_read.sum and dram__bytes_write.sum; remove an entry when its
 # kernel changes after the capture. Keys: (workload name, FP8 experts).
-# decode: 7.00 GB read, 4.45 MB written; FP8 decode: 3.50 GB, 3.34 MB; FP8 prefill:
-# 10.68 GB, 494.8 MB.
-TRAFFIC = {("decode", False): 7.00e9 + 4.45e6,
-           ("decode", True): 3.50e9 + 3.34e6, ("prefill", True): 10.68e9 + 494.8e6}
+TRAFFIC = {("decode", False): 7000938240 + 4401408, ("prefill", False): 19823741440 + 495698688,
+           ("decode", True): 3504753408 + 3475200, ("prefill", True): 10679746560 + 494778880}
 
 
 def peaks():
@@ -369,7 +367,7 @@ def main():
         secondary = {"workload": f"Beam prefill T={s_T}", "value": sec["value"], "unit": "tokens/s",
                      "ms_per_step": sec["ms_per_step"], "steps": s_steps, "roofline": sec["roofline"],
                      "layer_roofline": sec["layer_roofline"], "stage_ms": sec["stage_ms"],
-                     "n_touched_experts": sec["n_touched_experts"]}
+                     "n_touched_experts": sec["n_touched_experts"], "clocks": sec["clocks"]}
 
     fp8 = None
     if not args.no_secondary and name == "decode" and args.n_group == 8 and args.weights == "bf16":

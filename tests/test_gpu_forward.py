@@ -105,6 +105,25 @@ def test_forward_deterministic():
     assert torch.equal(a, c)
 
 
+@pytest.mark.parametrize("shape_name", ["tiny", "beam"])
+def test_small_and_large_dispatch_agree(shape_name, beam_experts):
+    """T = 128 runs the one-launch dispatch, T = 129 the four-launch one; every output row
+    depends only on its own token, so the first 128 rows must agree bit for bit."""
+    if shape_name == "tiny":
+        layer = tiny_layer(129, seed=9)
+        wg, wu, wd = layer.wg, layer.wu, layer.wd
+    else:
+        shape = W.BEAM
+        x = W.make_tokens(shape, 129, 9, "cuda")
+        wr, b = W.make_router(shape, 9, "cuda")
+        layer = P.Layer(shape, x, wr, b, *beam_experts)
+        wg, wu, wd = beam_experts
+    full = moe.forward(layer.x, layer.wr, layer.b, wg, wu, wd, layer.shape)
+    part = moe.forward(layer.x[:128].contiguous(), layer.wr, layer.b, wg, wu, wd, layer.shape)
+    abi.beam_moe_device_status()
+    assert torch.equal(full[:128], part)
+
+
 def test_zero_tokens_launch_nothing():
     layer = tiny_layer(1)
     out = torch.empty((1, layer.shape.d), dtype=torch.bfloat16, device="cuda")
