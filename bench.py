@@ -405,7 +405,9 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "flushed (512 MB write) before every timed step",
                        "expert_weights": "BF16" if args.weights == "bf16" else "FP8 E4M3, per-row FP32 scales"},
-            "roofline": {**res["roofline"], "peak_source": pk_src + " (MEASURED_PEAKS.json burst)"
+            "roofline": {**res["roofline"],
+                         "peak_source": (f"measured (MEASURED_PEAKS.json "
+                                         f"{'hbm_gbs, copy' if res['roofline']['bound'] == 'hbm' else 'bf16_tflops, burst'})")
                          if pk_src == "measured" else "fallback"},
             "layer_roofline": res["layer_roofline"],
             "stage_ms": res["stage_ms"],
