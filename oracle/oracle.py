@@ -272,6 +272,41 @@ class Oracle:
                 out[n] += w64[n, k] * self.expert_fp8(shape, xr, *experts_q(int(idx[n, k])))
         return out, idx
 
+    def forward_grouped(self, shape, x_bits, bias, experts, tokens, logits=None, router_w=None, idx_in=None):
+        """forward() for many tokens at Beam size: the same routing (this oracle's, from
+        `logits` if given), the same SwiGLU expert in FP64 with no intermediate rounding,
+        the same FP64 sum over each token's slots in slot order, but each expert evaluated
+        for all the tokens routed to it at once with numpy FP64 matrix products (a library
+        matmul as the step; equal to forward() up to the order of FP64 additions inside
+        the products). experts: callable e -> (wg_e, wu_e, wd_e) BF16 bit patterns.
+        Returns (out [n, d] FP64, idx [n, K] int32)."""
+        x_bits = _u16(x_bits)
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        lg = _f32(logits)[tokens] if logits is not None else self.router_logits(shape, x_bits[tokens], router_w)
+        idx, _, dbg = self.route(shape, lg, bias, debug=True)
+        w64 = dbg["w64"]
+        if idx_in is not None:
+            idx = np.asarray(idx_in, np.int32)
+            sc = dbg["s"].astype(np.float64)
+            picked = np.take_along_axis(sc, idx.astype(np.int64), axis=1)
+            w64 = shape.scale * picked / picked.sum(axis=1, keepdims=True)
+        n, K = idx.shape
+        xd = (x_bits[tokens].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        y = np.zeros((n, K, shape.d), np.float64)  # expert output of every (token, slot)
+        for e in np.unique(idx):
+            rows, slots = np.nonzero(idx == e)
+            wg, wu, wd = (((_u16(a).astype(np.uint32) << 16).view(np.float32)).astype(np.float64)
+                          for a in experts(int(e)))
+            xe = xd[rows]
+            g = xe @ wg.T
+            u = xe @ wu.T
+            h = g / (1.0 + np.exp(-g)) * u
+            y[rows, slots] = h @ wd.T
+        out = np.zeros((n, shape.d), np.float64)
+        for k in range(K):
+            out += w64[:, k:k + 1] * y[:, k]
+        return out, idx
+
     def forward_shard(self, shape, x_bits, bias, experts, e_begin, e_end, tokens, logits=None, router_w=None):
         """One expert-parallel shard's partial output for the rows `tokens`: the sum over the
         token's slots routed to experts [e_begin, e_end) of w_k * expert_k(x), FP64, with
@@ -341,6 +376,10 @@ def e4m3_decode(*a, **k):
 
 def expert_fp8(*a, **k):
     return default().expert_fp8(*a, **k)
+
+
+def forward_grouped(*a, **k):
+    return default().forward_grouped(*a, **k)
 
 
 def forward_fp8(*a, **k):

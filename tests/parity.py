@@ -102,22 +102,32 @@ def check_output(gpu_out, ref_out, what=""):
     return frob
 
 
-def oracle_forward_for(layer: Layer, tokens, gpu_logits_full, gpu_idx_full):
+def oracle_forward_for(layer: Layer, tokens, gpu_logits_full, gpu_idx_full, grouped=False):
     """Oracle output for `tokens` given the GPU's logits; near-tie tokens are rerun on the
-    GPU's selection. Returns (out [n, d] FP64, flagged tokens among `tokens`)."""
+    GPU's selection. grouped: evaluate with the oracle's grouped form (numpy FP64 products
+    per expert, for large token samples). Returns (out [n, d] FP64, flagged tokens among
+    `tokens`)."""
     shape = layer.shape
     tokens = np.asarray(tokens, np.int64)
     lg = gpu_logits_full[tokens]
-    idx_r, _, dbg = O.route(shape, lg, layer.b.cpu().numpy(), debug=True)
+    b = layer.b.cpu().numpy()
+    idx_r, _, dbg = O.route(shape, lg, b, debug=True)
     flagged_local = near_tie_tokens(shape, dbg)
     idx_in = np.asarray(gpu_idx_full[tokens], np.int32).copy()
     needed = set(np.unique(idx_in).tolist()) | set(np.unique(idx_r).tolist())
     xb = O.bf16_bits(layer.x)
-    out, _, _ = O.forward(shape, xb, layer.b.cpu().numpy(), layer.experts(needed), tokens=tokens,
-                          logits=gpu_logits_full)
+    experts = layer.experts(needed)
+    if grouped:
+        out, _ = O.forward_grouped(shape, xb, b, experts, tokens, logits=gpu_logits_full)
+    else:
+        out, _, _ = O.forward(shape, xb, b, experts, tokens=tokens, logits=gpu_logits_full)
     if len(flagged_local):
-        out2, _, _ = O.forward(shape, xb, layer.b.cpu().numpy(), layer.experts(needed), tokens=tokens[flagged_local],
-                               logits=gpu_logits_full, idx_in=idx_in[flagged_local])
+        if grouped:
+            out2, _ = O.forward_grouped(shape, xb, b, experts, tokens[flagged_local], logits=gpu_logits_full,
+                                        idx_in=idx_in[flagged_local])
+        else:
+            out2, _, _ = O.forward(shape, xb, b, experts, tokens=tokens[flagged_local], logits=gpu_logits_full,
+                                   idx_in=idx_in[flagged_local])
         out[flagged_local] = out2
     return out, tokens[flagged_local]
 

@@ -323,6 +323,28 @@ def pin_sublayer_composition(O, seed=15):
     np.testing.assert_allclose(out, want.numpy(), rtol=1e-9, atol=1e-9)
 
 
+def pin_forward_grouped_vs_per_token(O, seed=17):
+    """The grouped evaluation (numpy FP64 products per expert) equals the per-token C
+    forward, with the oracle's own routing and with a given selection."""
+    shape = W.TINY
+    x = W.make_tokens(shape, 48, seed, "cpu")
+    wr, b = W.make_router(shape, seed, "cpu")
+    wg, wu, wd = W.make_experts(shape, seed, "cpu")
+    xb = _bits(x)
+    host = {e: (_bits(wg[e]), _bits(wu[e]), _bits(wd[e])) for e in range(shape.E)}
+    experts = host.get
+    tokens = np.array([0, 3, 4, 9, 17, 30, 47])
+    logits = O.router_logits(shape, xb, wr.numpy())
+    ref, idx_r, _ = O.forward(shape, xb, b.numpy(), experts, tokens=tokens, logits=logits)
+    got, idx_g = O.forward_grouped(shape, xb, b.numpy(), experts, tokens, logits=logits)
+    assert np.array_equal(idx_r, idx_g)
+    assert np.abs(got - ref).max() <= 1e-12 * max(np.abs(ref).max(), 1.0)
+    sel = np.roll(idx_r, 1, axis=1)  # a different slot order of the same experts
+    ref2, _, _ = O.forward(shape, xb, b.numpy(), experts, tokens=tokens, logits=logits, idx_in=sel)
+    got2, _ = O.forward_grouped(shape, xb, b.numpy(), experts, tokens, logits=logits, idx_in=sel)
+    assert np.abs(got2 - ref2).max() <= 1e-12 * max(np.abs(ref2).max(), 1.0)
+
+
 def pin_e4m3_decoder_vs_torch(O):
     """Every FP8 E4M3 code decodes to torch's float8_e4m3fn value (NaN codes to NaN)."""
     q = np.arange(256, dtype=np.uint8)
@@ -357,5 +379,5 @@ ALL_CHECKS = [
     check_logits_vs_matmul, check_expert_vs_torch, check_forward_combination, check_zero_input,
     check_identical_experts, check_given_selection,
     pin_rmsnorm_library, pin_rmsnorm_closed_forms, pin_residual_is_scaled_sum, pin_round_bf16_vs_torch,
-    pin_sublayer_composition, pin_e4m3_decoder_vs_torch, pin_fp8_expert_vs_torch,
+    pin_sublayer_composition, pin_e4m3_decoder_vs_torch, pin_fp8_expert_vs_torch, pin_forward_grouped_vs_per_token,
 ]

@@ -22,7 +22,7 @@ def run_gpu(layer):
 
 def check_layer(layer, tokens, what):
     out, logits, idx = run_gpu(layer)
-    ref, flagged = P.oracle_forward_for(layer, tokens, logits, idx)
+    ref, flagged = P.oracle_forward_for(layer, tokens, logits, idx, grouped=len(tokens) > 64)
     frob = P.check_output(out[np.asarray(tokens)], ref, what)
     print(f"{what}: tokens checked {len(tokens)}, near-tie {len(flagged)}, rel frob {frob:.2e}")
     return out, idx
@@ -51,7 +51,7 @@ def test_tiny_forward_parity(T):
     ("sweep_T1024", 1024, 0, 16),
     ("prefill", 4096, 0, 32),
     ("sweep_T16384", 16384, 0, 16),
-    ("skewed", 32768, 16, 48),
+    ("skewed", 32768, 16, 1024),   # the oracle checks a seeded 1024-token subset
 ])
 def test_beam_forward_parity(beam_experts, beam_host_cache, name, T, hot, n_check):
     shape = W.BEAM
