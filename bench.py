@@ -1,7 +1,7 @@
 """Benchmark of the Beam routed-MoE forward pass (libbeam_moe.so) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|tiny|T<n>]
-                    [--impl reference] [--no-secondary] [--weights bf16|fp8]
+                    [--impl reference] [--no-secondary] [--weights bf16|fp8] [--sweep]
 
 A step is one beam_moe_forward call over one batch of T tokens: router, dispatch,
 gate/up GEMM with SwiGLU, down GEMM, combine. Inputs and weights are synthetic, seeded,
@@ -314,6 +314,8 @@ def main():
     ap.add_argument("--oracle-tokens", type=int, default=None)
     ap.add_argument("--n-group", type=int, default=8, help="expert groups of 32 (8 = Beam); fewer for profiling")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"], help="expert weights of the headline")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also measure the token-count sweep T in {1, 8, 64, 256, 1024, 4096, 16384} (BF16)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -385,6 +387,21 @@ def main():
                            "stage_ms": r["stage_ms"], "clocks": r["clocks"]}
         del experts_fp8
 
+    sweep = None
+    if args.sweep and args.n_group == 8:
+        sweep = []
+        for sT in (1, 8, 64, 256, 1024, 4096, 16384):
+            s_name, s_shape, _, _ = workload(f"T{sT}")
+            s_steps = max(10, min(args.steps, 30))
+            r = measure(s_name, s_shape, sT, 0, s_steps, args.warmup, experts, device, flush, pk, e2e=False)
+            lr = r["layer_roofline"]
+            sweep.append({"T": sT, "value": r["value"], "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
+                          "layer_bound": "hbm" if lr["bytes"] / (pk["hbm_gbs"] * 1e9) >=
+                                         lr["flops"] / (pk["bf16_tflops"] * 1e12) else "tensor",
+                          "layer_roofline_frac": lr["frac"], "tensor_frac_of_burst": lr["tensor_frac_of_burst"],
+                          "expert_mlp": {k: r["roofline"][k] for k in ("bound", "achieved", "unit", "frac", "kernel_ms")},
+                          "n_touched_experts": r["n_touched_experts"], "clocks": r["clocks"]})
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x, wr, b, (wg, wu, wd) = make_layer(shape, T, hot, device, experts)
@@ -421,6 +438,8 @@ def main():
             line["secondary"] = secondary
         if fp8:
             line["fp8_experts"] = fp8
+        if sweep:
+            line["sweep"] = sweep
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
