@@ -221,6 +221,16 @@ BEAM_MOE_API const char *beam_moe_last_error(void);
  * 2 = a pipeline wait in a GEMM ran past its limit). */
 BEAM_MOE_API int beam_moe_device_status(cudaStream_t stream);
 
+/* Self-test of failure detection (no counterpart on the pages). Runs the expert kernel on a
+ * library-built one-tile work list (one expert, d = I = 128, zero weights) whose completion
+ * counter is set far below zero, so the down item's producer waits out its bounded wait
+ * (2 s), records "a GEMM pipeline wait ran past its limit" in the device status word, and
+ * its CTA drains its copies and MMAs and frees its tensor memory before exiting. Returns
+ * BEAM_MOE_OK once the work is queued on `stream`; a following beam_moe_device_status()
+ * then returns BEAM_MOE_ERR_DEVICE (and clears the word), and the context stays usable.
+ * Takes about two seconds of GPU time. */
+BEAM_MOE_API int beam_moe_selftest_wait_timeout(cudaStream_t stream);
+
 /* Per-stage timing for profiling. While enabled (per thread), each forward/route call
  * records CUDA events on its stream around each stage; beam_moe_timing_read synchronises
  * on the last call's final event and writes up to max_stages durations in milliseconds

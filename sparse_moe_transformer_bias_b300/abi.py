@@ -32,7 +32,7 @@ EXPORTS = ("beam_moe_default_config", "beam_moe_route", "beam_moe_route_ex", "be
            "beam_moe_forward_ex", "beam_moe_router_logits", "beam_moe_last_error", "beam_moe_device_status",
            "beam_moe_timing_enable", "beam_moe_timing_read", "beam_moe_last_launch_count",
            "beam_moe_route_noalloc", "beam_moe_rmsnorm", "beam_moe_sublayer_forward", "beam_moe_forward_shard",
-           "beam_moe_dense_mlp", "beam_moe_forward_fp8")
+           "beam_moe_dense_mlp", "beam_moe_forward_fp8", "beam_moe_selftest_wait_timeout")
 
 
 class BeamMoeConfig(ctypes.Structure):
@@ -79,6 +79,7 @@ def load() -> ctypes.CDLL:
             L.beam_moe_forward_shard.argtypes = [cfgp, P, P, P, P, P, P, i, i, i, P, P]
             L.beam_moe_dense_mlp.argtypes = [i, i, P, P, P, P, i, P, P]
             L.beam_moe_forward_fp8.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i, P, P]
+            L.beam_moe_selftest_wait_timeout.argtypes = [P]
             L.beam_moe_last_error.restype = ctypes.c_char_p
             L.beam_moe_last_error.argtypes = []
             L.beam_moe_device_status.argtypes = [P]
@@ -89,7 +90,7 @@ def load() -> ctypes.CDLL:
                       "beam_moe_router_logits", "beam_moe_device_status", "beam_moe_timing_enable",
                       "beam_moe_timing_read", "beam_moe_last_launch_count", "beam_moe_route_noalloc",
                       "beam_moe_rmsnorm", "beam_moe_sublayer_forward", "beam_moe_forward_shard",
-                      "beam_moe_dense_mlp", "beam_moe_forward_fp8"):
+                      "beam_moe_dense_mlp", "beam_moe_forward_fp8", "beam_moe_selftest_wait_timeout"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -167,6 +168,12 @@ def beam_moe_forward_fp8(cfg, x, router_w, expert_bias, w_gate_q, gate_scale, w_
     return _check(load().beam_moe_forward_fp8(_cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate_q),
                                               _ptr(gate_scale), _ptr(w_up_q), _ptr(up_scale), _ptr(w_down_q),
                                               _ptr(down_scale), int(T), _ptr(out), _stream(stream)))
+
+
+def beam_moe_selftest_wait_timeout(stream=None):
+    """Queue the failure-detection self-test (a bounded wait that runs out); read the
+    outcome with beam_moe_device_status()."""
+    return _check(load().beam_moe_selftest_wait_timeout(_stream(stream)))
 
 
 def beam_moe_dense_mlp(d, I, x, w_gate, w_up, w_down, T, out, stream=None):

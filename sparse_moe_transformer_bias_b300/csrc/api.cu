@@ -470,6 +470,53 @@ done:
     return rc;
 }
 
+int beam_moe_selftest_wait_timeout(cudaStream_t stream) {
+    g_launches = 0;
+    timing_begin_call();
+    int rc;
+    if ((rc = check_stream(stream))) return rc;
+    DeviceState* dev = nullptr;
+    if ((rc = device_state(&dev))) return rc;
+    // One expert of d = I = 128, one N-tile of 16 of 32 rows: one gate/up item, one down item.
+    const Shape s{128, 128, 1, 1, 1, 1, 1.0f};
+    const int rows = 32, T = 16, bn_max = 32;
+    const int max_tiles = dense_max_tiles(T, bn_max);
+    Carver c{nullptr};
+    c.take<bf16>(3 * 128 * 128);
+    c.take<bf16>(3 * static_cast<size_t>(rows) * 128);
+    c.take<int4>(1 + static_cast<size_t>(max_tiles));
+    c.take<int>(static_cast<size_t>(max_tiles));
+    const size_t bytes = c.off + 256;
+    void* mem = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, stream);
+    if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "scratch allocation of %zu bytes: %s", bytes, cudaGetErrorString(e));
+    Carver cc{static_cast<char*>(mem)};
+    bf16* w = cc.take<bf16>(3 * 128 * 128);
+    bf16* act = cc.take<bf16>(3 * static_cast<size_t>(rows) * 128);
+    int4* tiles = cc.take<int4>(1 + static_cast<size_t>(max_tiles));
+    int* tile_done = cc.take<int>(static_cast<size_t>(max_tiles));
+    const cudaStream_t st = stream;
+    rc = BEAM_MOE_OK;
+    if ((e = cudaMemsetAsync(mem, 0, bytes, st)) != cudaSuccess) {
+        rc = fail(BEAM_MOE_ERR_CUDA, "scratch clear: %s", cudaGetErrorString(e));
+        goto done;
+    }
+    LAUNCH(kCount, launch_dense_tiles(T, bn_max, tiles, tile_done, st));
+    // The tile's completion counter starts far below zero, so the gate/up epilogue can never
+    // raise it to the count the down item waits for.
+    if ((e = cudaMemsetAsync(tile_done, 0x80, sizeof(int), st)) != cudaSuccess) {
+        rc = fail(BEAM_MOE_ERR_CUDA, "counter poison: %s", cudaGetErrorString(e));
+        goto done;
+    }
+    LAUNCH(kExpert, launch_expert_mlp(s, w, w + 128 * 128, w + 2 * 128 * 128, act, rows, tiles, tile_done, max_tiles,
+                                      bn_max, act + rows * 128, act + 2 * rows * 128, dev->status, dev->num_sms, st));
+done:
+    e = cudaFreeAsync(mem, stream);
+    if (rc == BEAM_MOE_OK && e != cudaSuccess)
+        rc = fail(BEAM_MOE_ERR_CUDA, "scratch release: %s", cudaGetErrorString(e));
+    return rc;
+}
+
 int beam_moe_rmsnorm(int d, const __nv_bfloat16* v, const __nv_bfloat16* gamma, float eps, int T,
                      __nv_bfloat16* out, cudaStream_t stream) {
     g_launches = 0;
