@@ -22,8 +22,9 @@
 // rows than one N-tile holds has its N-tiles' items of the same weight tile handed out
 // together, so the CTAs running them stream those weights at the same time and the
 // repeats are served by L2 instead of HBM (those weight loads carry the normal L2
-// priority; weights read once carry evict-first). A down item of tile n reads h rows that the gate/up items of tile n write:
-// each epilogue warp of a gate/up item increments tile_done[n] after its stores, and the
+// priority; weights read once carry evict-first).
+// A down item of tile n reads h rows that the gate/up items of tile n write: each
+// epilogue warp of a gate/up item increments tile_done[n] after its stores, and the
 // producer of a down item waits (bounded) until tile_done[n] counts every warp of every
 // gate/up item of the tile. All gate/up ids are handed out before any down id, and a
 // producer only waits after it has issued every copy of its earlier items, so the MMAs
@@ -41,7 +42,8 @@
 //   warps 2..9:    epilogue - tcgen05.ld of their TMEM lane quarter, two warps per quarter
 //                  taking alternate 16-column granules.
 // TMEM is a ring of accumulator slots of kBNMax columns; every item takes two, so with
-// four slots (kBNMax <= 128) the epilogue of one item overlaps the MMAs of the next.
+// four slots (kBNMax <= 128) the epilogue of one item overlaps the MMAs of the next (two
+// slots at 192 and 256 rows).
 // Every wait is bounded (2 s); on expiry the CTA records kStatusWaitTimeout, the roles
 // leave their loops, copies and MMAs already issued are drained (bounded), and TMEM is
 // freed before the CTA exits.
@@ -51,12 +53,13 @@
 // swizzle; as many bytes per copy as a BF16 tile) and the token rows as two 64-wide BF16
 // halves; eight converter warps (two per TMEM lane quarter, one per weight tile of the
 // stage) widen each row's 128 codes and store them with tcgen05.st into a ring of A
-// buffers in TMEM, and the MMA reads A from TMEM (B, the token rows, from shared memory). The widening is
-// exact: E4M3 -> F16 by cvt (every finite code is an F16 normal or zero), then F16 -> BF16
-// by moving the exponent and mantissa bits down three places, which keeps every bit and
-// multiplies the value by 2^-112 (zero stays zero; every nonzero code lands on a BF16
-// normal). The epilogue multiplies each accumulator by 2^112 and then by its row's scale,
-// so the products are those of W[r][c] = scale[r] * e4m3(q[r][c]) with FP32 accumulation.
+// buffers in TMEM, and the MMA reads A from TMEM (B, the token rows, from shared memory).
+// The widening is exact: E4M3 -> F16 by cvt (every finite code is an F16 normal or zero),
+// then F16 -> BF16 by moving the exponent and mantissa bits down three places, which
+// keeps every bit and multiplies the value by 2^-112 (zero stays zero; every nonzero code
+// lands on a BF16 normal). The epilogue multiplies each accumulator by 2^112 and then by
+// its row's scale, so the products are those of W[r][c] = scale[r] * e4m3(q[r][c]) with
+// FP32 accumulation.
 #include "internal.cuh"
 #include "ptx.cuh"
 
