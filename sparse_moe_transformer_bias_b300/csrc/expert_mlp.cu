@@ -83,9 +83,13 @@ struct MlpCfg {
     static constexpr int kStage = 2 * kA + kB;
     static constexpr int kBudget = 227 * 1024 - 2048;
     static constexpr int kStages = (kBudget / kStage) > 10 ? 10 : (kBudget / kStage);
-    // FP8: a ring of converted A buffers in TMEM, each the stage's two weight tiles as BF16
-    // (2 x 64 columns), after the accumulator slots.
-    static constexpr int kACols = kFP8 ? 2 * kKStage / 2 : 0;
+    // FP8: a ring of converted A buffers in TMEM after the accumulator slots. A buffer holds
+    // kAK of K of the stage's two weight tiles as BF16 (2 x kAK/2 columns): the whole stage
+    // (K = 128) up to 128-row tiles; half of it (K = 64, two buffers per stage) at 192 rows,
+    // where the accumulators leave 128 columns.
+    static constexpr int kAParts = kFP8 ? (kBNMax > 128 ? 2 : 1) : 1;
+    static constexpr int kAK = kKStage / kAParts;
+    static constexpr int kACols = kFP8 ? kAK : 0;
     static constexpr int kABufs = kFP8 ? (kBNMax <= 32 ? 3 : 2) : 0;
     static constexpr int kAccCols = 512 - kABufs * kACols;
     static constexpr int kSlots = ((kAccCols / kBNMax) < 4 ? (kAccCols / kBNMax) : 4) & ~1;  // items take pairs
@@ -393,39 +397,48 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                         ok = false;
                         break;
                     }
-                    if constexpr (kFP8) {
-                        if (!ptx::mbar_wait(bar(AFULL0 + abuf), aphase, abort_flag, kWaitLimitNs)) {
-                            ok = false;
-                            break;
-                        }
-                    }
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_u32(smem + stage * C::kStage);
                     const uint32_t sb = sa + 2 * C::kA;
+                    constexpr int kPerRow = kTileK / kMmaK;  // K steps per 128-byte swizzle row
+                    if constexpr (kFP8) {
+                        // kAParts A buffers per stage, each kAK of K
+                        for (int part = 0; part < C::kAParts && ok; ++part) {
+                            if (!ptx::mbar_wait(bar(AFULL0 + abuf), aphase, abort_flag, kWaitLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            const uint32_t ta0 = tmem_base + C::kABase + abuf * C::kACols;
 #pragma unroll
-                    for (int kk = 0; kk < C::kKStage / kMmaK; ++kk) {
-                        constexpr int kPerRow = kTileK / kMmaK;  // K steps per 128-byte swizzle row
-                        const uint64_t bdesc =
-                            ptx::sw128_kmajor_desc(sb + (kk / kPerRow) * C::kBHalf + (kk % kPerRow) * kMmaK * 2);
-                        const uint32_t accum = (kc | kk) ? 1u : 0u;
-                        if constexpr (kFP8) {
-                            const uint32_t ta = tmem_base + C::kABase + abuf * C::kACols + kk * (kMmaK / 2);
-                            ptx::mma_bf16_ta(d0, ta, bdesc, idesc, accum);
-                            ptx::mma_bf16_ta(d1, ta + C::kKStage / 2, bdesc, idesc, accum);
-                        } else {
+                            for (int kk = 0; kk < C::kAK / kMmaK; ++kk) {
+                                const int g = part * (C::kAK / kMmaK) + kk;  // K step within the stage
+                                const uint64_t bdesc =
+                                    ptx::sw128_kmajor_desc(sb + (g / kPerRow) * C::kBHalf + (g % kPerRow) * kMmaK * 2);
+                                const uint32_t accum = (kc | g) ? 1u : 0u;
+                                const uint32_t ta = ta0 + kk * (kMmaK / 2);
+                                ptx::mma_bf16_ta(d0, ta, bdesc, idesc, accum);
+                                ptx::mma_bf16_ta(d1, ta + C::kAK / 2, bdesc, idesc, accum);
+                            }
+                            ptx::mma_commit(bar(AEMPTY0 + abuf));
+                            if (++abuf == C::kABufs) {
+                                abuf = 0;
+                                aphase ^= 1;
+                            }
+                        }
+                        if (!ok) break;
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < C::kKStage / kMmaK; ++kk) {
+                            const uint64_t bdesc =
+                                ptx::sw128_kmajor_desc(sb + (kk / kPerRow) * C::kBHalf + (kk % kPerRow) * kMmaK * 2);
+                            const uint32_t accum = (kc | kk) ? 1u : 0u;
                             ptx::mma_bf16(d0, ptx::sw128_kmajor_desc(sa + kk * kMmaK * 2), bdesc, idesc, accum);
                             ptx::mma_bf16(d1, ptx::sw128_kmajor_desc(sa + C::kA + kk * kMmaK * 2), bdesc, idesc,
                                           accum);
                         }
                     }
                     ptx::mma_commit(bar(EMPTY0 + stage));
-                    if constexpr (kFP8) {
-                        ptx::mma_commit(bar(AEMPTY0 + abuf));
-                        if (++abuf == C::kABufs) {
-                            abuf = 0;
-                            aphase ^= 1;
-                        }
-                    }
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -475,41 +488,46 @@ __global__ void __launch_bounds__(kThreadsFor(kFP8), 1)
                 if (!it.ok || it.tl.z > kBNMax) continue;
                 const int k_chunks = it.down ? args.kc_dn : args.kc_gu;
                 for (int kc = 0; kc < k_chunks; ++kc) {
-                    if (!ptx::mbar_wait(bar(FULL0 + stage), phase, abort_flag, kWaitLimitNs) ||
-                        !ptx::mbar_wait(bar(AEMPTY0 + abuf), aphase ^ 1, abort_flag, kWaitLimitNs)) {
+                    if (!ptx::mbar_wait(bar(FULL0 + stage), phase, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                    ptx::tc_fence_after();
                     const uint8_t* src = smem + stage * C::kStage + t * C::kA + r * C::kKStage;
-                    const uint32_t dst = tmem_base + lane_off + C::kABase + abuf * C::kACols + t * (C::kKStage / 2);
-#pragma unroll
-                    for (int part = 0; part < C::kKStage / 64; ++part) {  // 64 codes -> 32 columns
-                        uint4 v[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            v[j] = *reinterpret_cast<const uint4*>(src + 16 * ((4 * part + j) ^ swz));
-                        uint32_t o[32];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            e4m3x4_to_bf16x4_scaled(v[j].x, o[8 * j + 0], o[8 * j + 1]);
-                            e4m3x4_to_bf16x4_scaled(v[j].y, o[8 * j + 2], o[8 * j + 3]);
-                            e4m3x4_to_bf16x4_scaled(v[j].z, o[8 * j + 4], o[8 * j + 5]);
-                            e4m3x4_to_bf16x4_scaled(v[j].w, o[8 * j + 6], o[8 * j + 7]);
+                    for (int part = 0; part < C::kAParts; ++part) {  // one A buffer: kAK codes per row
+                        if (!ptx::mbar_wait(bar(AEMPTY0 + abuf), aphase ^ 1, abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
                         }
-                        ptx::tmem_st32(dst + 32 * part, o);
+                        ptx::tc_fence_after();
+                        const uint32_t dst = tmem_base + lane_off + C::kABase + abuf * C::kACols + t * (C::kAK / 2);
+#pragma unroll
+                        for (int sub = 0; sub < C::kAK / 64; ++sub) {  // 64 codes -> 32 columns
+                            const int c0 = 4 * (part * (C::kAK / 64) + sub);  // first 16-byte chunk
+                            uint4 v[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                v[j] = *reinterpret_cast<const uint4*>(src + 16 * ((c0 + j) ^ swz));
+                            uint32_t o[32];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                e4m3x4_to_bf16x4_scaled(v[j].x, o[8 * j + 0], o[8 * j + 1]);
+                                e4m3x4_to_bf16x4_scaled(v[j].y, o[8 * j + 2], o[8 * j + 3]);
+                                e4m3x4_to_bf16x4_scaled(v[j].z, o[8 * j + 4], o[8 * j + 5]);
+                                e4m3x4_to_bf16x4_scaled(v[j].w, o[8 * j + 6], o[8 * j + 7]);
+                            }
+                            ptx::tmem_st32(dst + 32 * sub, o);
+                        }
+                        ptx::tmem_wait_st();
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(bar(AFULL0 + abuf));
+                        if (++abuf == C::kABufs) {
+                            abuf = 0;
+                            aphase ^= 1;
+                        }
                     }
-                    ptx::tmem_wait_st();
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::mbar_arrive(bar(AFULL0 + abuf));
-                        ptx::mbar_arrive(bar(EMPTY0 + stage));
-                    }
-                    if (++abuf == C::kABufs) {
-                        abuf = 0;
-                        aphase ^= 1;
-                    }
+                    if (!ok) break;
+                    if (lane == 0) ptx::mbar_arrive(bar(EMPTY0 + stage));  // this tile's codes are read
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -668,7 +686,7 @@ int gemm_bn_max(const Shape& s, int T) {
 
 int gemm_bn_max_fp8(const Shape& s, int T) {
     const int b = gemm_bn_max(s, T);
-    return b < 128 ? b : 128;
+    return b < 192 ? b : 192;
 }
 
 namespace {
@@ -753,7 +771,7 @@ cudaError_t launch_expert_mlp(const Shape& s, const bf16* w_gate, const bf16* w_
 cudaError_t launch_expert_mlp_fp8(const Shape& s, const Fp8Experts& q, const bf16* x_perm, int rows,
                                   const int4* tiles, int* tile_done, int max_tiles, int bn_max, bf16* h, bf16* y,
                                   int* status, int num_sms, cudaStream_t st) {
-    if (bn_max > 128) return cudaErrorInvalidValue;
+    if (bn_max > 192) return cudaErrorInvalidValue;
     CUtensorMap wg, wu, wd;
     BMaps bx, bh;
     const char* why = nullptr;
@@ -769,7 +787,8 @@ cudaError_t launch_expert_mlp_fp8(const Shape& s, const Fp8Experts& q, const bf1
     a.ds = q.ds;
     const int grid = mlp_grid(a, max_tiles, num_sms);
     if (bn_max <= 32) return launch_mlp<32, true>(wg, wu, wd, bx, bh, a, grid, st);
-    return launch_mlp<128, true>(wg, wu, wd, bx, bh, a, grid, st);
+    if (bn_max <= 128) return launch_mlp<128, true>(wg, wu, wd, bx, bh, a, grid, st);
+    return launch_mlp<192, true>(wg, wu, wd, bx, bh, a, grid, st);
 }
 
 }  // namespace beam

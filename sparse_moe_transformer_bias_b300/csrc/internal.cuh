@@ -111,7 +111,7 @@ struct Fp8Experts {
     const float* ds;
 };
 // Largest N-tile of the FP8 expert kernel (its converted weights share TMEM with the
-// accumulators, so tiles stop at 128 rows).
+// accumulators, so tiles stop at 192 rows).
 int gemm_bn_max_fp8(const Shape& s, int T);
 // The expert kernel on FP8 weights: the same items and outputs as launch_expert_mlp, the
 // weight tiles widened to BF16 on chip and the accumulators scaled per weight row.

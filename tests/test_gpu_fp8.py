@@ -42,7 +42,7 @@ def tiny_fp8():
     return W.make_experts_fp8(W.TINY, seed=0, device="cuda")
 
 
-@pytest.mark.parametrize("T", [1, 16, 33, 129, 300])
+@pytest.mark.parametrize("T", [1, 16, 33, 129, 300, 1500])
 def test_tiny_fp8_parity(tiny_fp8, T):
     shape = W.TINY
     x = W.make_tokens(shape, T, 0, "cuda")
