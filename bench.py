@@ -223,9 +223,12 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
         "value": T * steps / (total_ms * 1e-3),
         "ms_per_step": ms_per_step,
         "roofline": roof,
+        "ms_per_step_median": statistics.median(step_ms),
         "layer_roofline": {"t_roof_ms": t_roof_s * 1e3, "frac": t_roof_s * 1e3 / ms_per_step,
                            "flops": layer_flops, "bytes": layer_bytes,
-                           "tensor_frac_of_burst": layer_flops / (pk["bf16_tflops"] * 1e12) / (ms_per_step * 1e-3)},
+                           "tensor_frac_of_burst": layer_flops / (pk["bf16_tflops"] * 1e12) / (ms_per_step * 1e-3),
+                           "tensor_frac_of_sustained":
+                               layer_flops / (pk["bf16_tflops_sustained"] * 1e12) / (ms_per_step * 1e-3)},
         "stage_ms": stage_ms,
         "n_touched_experts": n_touched,
         "gpu_launches": launches * steps,
@@ -413,6 +416,7 @@ def main():
         line = {
             "metric": METRIC, "value": res["value"] * world, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+            "ms_per_step_median": res["ms_per_step_median"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) FP32 router, U(-0.1,0.1) bias, "
                     "BF16 experts std 1/sqrt(fan_in))",
