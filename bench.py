@@ -260,8 +260,30 @@ def measure_e2e(shape, T, x, wr, b, wg, wu, wd, steps, warmup, flush):
                          stream=stream)
         total += time.perf_counter() - t0
     total = max_over_ranks(total * 1e3) * 1e-3
-    return {"value": T * steps / total, "unit": "tokens/s", "h2d_bytes_per_step": T * shape.d * 2,
-            "d2h_bytes_per_step": T * shape.d * 2, "timer": "host wall clock around each synchronous step"}
+    res = {"value": T * steps / total, "unit": "tokens/s", "h2d_bytes_per_step": T * shape.d * 2,
+           "d2h_bytes_per_step": T * shape.d * 2, "timer": "host wall clock around each synchronous step"}
+    # The same through moe.ForwardGraph: the call captured once, replayed per step.
+    g = moe.ForwardGraph(x_dev, wr, b, wg, wu, wd, shape, out=out_dev)
+    stream = torch.cuda.current_stream()
+
+    def graph_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        g.replay()
+        out_host.copy_(out_dev, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(warmup):
+        graph_step()
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        graph_step()
+        total += time.perf_counter() - t0
+    total = max_over_ranks(total * 1e3) * 1e-3
+    res["graph"] = {"value": T * steps / total, "unit": "tokens/s", "call": "moe.ForwardGraph.replay"}
+    return res
 
 
 # ---------------------------------------------------------------- CPU oracle arm

@@ -66,6 +66,11 @@ int device_state(DeviceState** out) {
 
 int check_stream(cudaStream_t st) {
     if (st == nullptr) return BEAM_MOE_OK;
+    // While the stream is being captured into a graph the device query below is not
+    // allowed; the launches are recorded on the capturing stream as they are.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusActive) return BEAM_MOE_OK;
+    cudaGetLastError();
     int sdev = -1, cdev = -1;
     if (cudaStreamGetDevice(st, &sdev) != cudaSuccess || cudaGetDevice(&cdev) != cudaSuccess) {
         cudaGetLastError();

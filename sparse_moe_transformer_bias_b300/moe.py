@@ -142,3 +142,29 @@ def dense_mlp(x, w_gate, w_up, w_down, out=None, stream=None):
         out = torch.empty_like(x)
     abi.beam_moe_dense_mlp(d, I, x, w_gate, w_up, w_down, T, out, stream)
     return out
+
+
+class ForwardGraph:
+    """beam_moe_forward captured once in a CUDA graph for fixed device buffers and replayed:
+    one graph launch instead of the call's kernel launches and scratch allocation. Write
+    new tokens into `x` (same shape) before each replay; the result lands in `out`. The
+    weights, router and bias must stay at the same addresses."""
+
+    def __init__(self, x, router_w, bias, w_gate, w_up, w_down, shape: MoEShape = BEAM, out=None):
+        self.x = x
+        self.out = out if out is not None else torch.empty((x.shape[0], shape.d), dtype=torch.bfloat16,
+                                                           device=x.device)
+        args = (router_w, bias, w_gate, w_up, w_down, shape)
+        side = torch.cuda.Stream(device=x.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # the library's per-device state and pool exist before capture
+            forward(self.x, *args, out=self.out, stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            forward(self.x, *args, out=self.out, stream=torch.cuda.current_stream())
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
+
