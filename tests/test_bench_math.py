@@ -1,0 +1,39 @@
+"""The benchmark's roofline arithmetic against its definitions (no GPU): layer FLOPs
+T * (top_k * 3 * 2 * d * I + 2 * d * E); bytes of the touched experts' weights once (BF16:
+2 bytes per weight; FP8: 1 byte per weight plus one FP32 scale per weight row), the router,
+bias, tokens in and out, and the routing outputs; the expert kernel's bytes add its
+activation traffic."""
+import bench
+from sparse_moe_transformer_bias_b300 import workloads as W
+
+
+def test_layer_flops_and_bytes_bf16():
+    s = W.BEAM
+    T, n, rows = 16, 89, 128
+    flops, bytes_, kern = bench.algorithmic(s, T, n, rows)
+    assert flops == T * (8 * 3 * 2 * 5120 * 2560 + 2 * 5120 * 256)
+    assert abs(flops / T - 631.77e6) < 0.01e6                     # per-token figure of the layer
+    per_expert = 3 * 5120 * 2560 * 2
+    assert per_expert == 78_643_200
+    assert bytes_ == n * per_expert + 256 * 5120 * 4 + 256 * 4 + 2 * T * 5120 * 2 + T * 8 * 8
+    mlp = kern["expert_mlp"]
+    assert mlp["flops"] == 2 * rows * 5120 * 2560 * 3
+    assert mlp["bytes"] == n * per_expert + rows * (5120 * 2 + 2 * 2560 * 2 + 5120 * 2)
+
+
+def test_fp8_bytes_count_codes_and_row_scales():
+    s = W.BEAM
+    _, bytes8, kern8 = bench.algorithmic(s, 16, 89, 128, fp8=True)
+    _, bytes16, _ = bench.algorithmic(s, 16, 89, 128)
+    per_expert8 = 3 * 5120 * 2560 + (2 * 2560 + 5120) * 4
+    assert bytes16 - bytes8 == 89 * (3 * 5120 * 2560 * 2 - per_expert8)
+    assert kern8["expert_mlp"]["bytes"] == 89 * per_expert8 + 128 * (5120 * 2 + 2 * 2560 * 2 + 5120 * 2)
+
+
+def test_single_process_helpers():
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.rank_world() == (0, 1, 0)
+    name, shape, T, hot = bench.workload("prefill")
+    assert (name, T, hot, shape.E) == ("prefill", 4096, 0, 256)
+    name, shape, T, _ = bench.workload("decode", n_group=1)
+    assert (name, shape.E, shape.topk_group, T) == ("decode_E32", 32, 1, 16)
