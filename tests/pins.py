@@ -373,6 +373,78 @@ def pin_fp8_expert_vs_torch(O, seed=16):
     assert float((want - ref).norm() / ref.norm()) < 0.08
 
 
+
+def _pow2_fp8_experts(shape, seed):
+    """FP8 experts whose dequantised weights are exact BF16 values: per-row scales that are
+    powers of two (2^ceil(log2(absmax / 448))), codes rounded to E4M3 by torch. An E4M3
+    value has at most 4 significant bits, so scale * value is a BF16 number. Returns the
+    codes and scales as ((gq, gs), (uq, us), (dq, ds)) and the equal BF16 experts."""
+    g = torch.Generator().manual_seed(seed)
+    fp8, bf = [], []
+    for rows, cols in ((shape.I, shape.d), (shape.I, shape.d), (shape.d, shape.I)):
+        w = torch.randn((shape.E, rows, cols), generator=g, dtype=torch.float64) / math.sqrt(cols)
+        amax = w.abs().amax(dim=-1).clamp_min(1e-30)
+        sc = torch.exp2(torch.ceil(torch.log2(amax / W.FP8_MAX))).float()
+        q = (w / sc.double().unsqueeze(-1)).float().to(torch.float8_e4m3fn)
+        deq = q.to(torch.float64) * sc.double().unsqueeze(-1)
+        wb = deq.to(torch.bfloat16)
+        assert torch.equal(wb.double(), deq), "a power-of-two-scaled E4M3 weight must be a BF16 value"
+        fp8.append((q.view(torch.uint8), sc))
+        bf.append(wb)
+    return tuple(fp8), tuple(bf)
+
+
+def pin_forward_fp8_equals_bf16_block(orc, seed=18):
+    """The FP8 block's composition (routing, weights, slot sum) against the BF16 block: on
+    FP8 experts whose dequantised weights are exactly BF16 values, forward_fp8 must equal
+    forward on those BF16 weights, both with the oracle's own routing and with a selection
+    handed in (weights re-derived from the unbiased sigmoid scores)."""
+    shape = W.MoEShape(d=64, I=48)  # Beam's routing (256 experts, 8 groups, top 4, top 8), narrow experts
+    T = 6
+    x = W.make_tokens(shape, T, seed)
+    wr, b = W.make_router(shape, seed)
+    ((gq, gs), (uq, us), (dq, ds)), (wg, wu, wd) = _pow2_fp8_experts(shape, seed)
+    xb = _bits(x)
+    experts_q = lambda e: (gq[e].numpy(), gs[e].numpy(), uq[e].numpy(), us[e].numpy(), dq[e].numpy(),  # noqa: E731
+                           ds[e].numpy())
+    experts_b = lambda e: (_bits(wg[e]), _bits(wu[e]), _bits(wd[e]))  # noqa: E731
+    tokens = np.arange(T)
+    logits = orc.router_logits(shape, xb, wr.numpy())
+    ref, idx_r, _ = orc.forward(shape, xb, b.numpy(), experts_b, tokens=tokens, logits=logits)
+    got, idx_g = orc.forward_fp8(shape, xb, b.numpy(), experts_q, tokens, logits=logits)
+    np.testing.assert_array_equal(idx_g, idx_r)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    # a selection from outside, in another slot order, with experts the router did not pick
+    sel = np.roll(idx_r, 3, axis=1).copy()
+    sel[:, 0] = (sel[:, 0] + 101) % shape.E
+    for t in range(T):
+        assert len(set(sel[t].tolist())) == shape.top_k
+    ref2, _, _ = orc.forward(shape, xb, b.numpy(), experts_b, tokens=tokens, logits=logits, idx_in=sel)
+    got2, idx2 = orc.forward_fp8(shape, xb, b.numpy(), experts_q, tokens, logits=logits, idx_in=sel)
+    np.testing.assert_array_equal(idx2, sel)
+    np.testing.assert_allclose(got2, ref2, rtol=1e-12, atol=1e-12 * np.abs(ref2).max())
+
+
+def pin_forward_fp8_identical_experts(orc, seed=19):
+    """Closed form for the FP8 block: when every expert is the same FP8 expert, the routed
+    weights sum to the scale and the output is scale * expert_fp8(x), whatever the routing
+    (router weights drawn from the Tiny recipe, FP8 experts from the quantisation recipe)."""
+    shape = W.TINY
+    T = 5
+    x = W.make_tokens(shape, T, seed)
+    wr, b = W.make_router(shape, seed)
+    (gq, gs), (uq, us), (dq, ds) = W.make_experts_fp8(shape, seed)
+    e0 = 9
+    one = (gq[e0].numpy(), gs[e0].numpy(), uq[e0].numpy(), us[e0].numpy(), dq[e0].numpy(), ds[e0].numpy())
+    out, _ = orc.forward_fp8(shape, _bits(x), b.numpy(), lambda e: one, np.arange(T), router_w=wr.numpy())
+    # the single expert from torch float64 on the dequantised weights
+    deq = lambda q, sc: torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64) \
+        * torch.from_numpy(sc).double().unsqueeze(1)  # noqa: E731
+    wg64, wu64, wd64 = deq(one[0], one[1]), deq(one[2], one[3]), deq(one[4], one[5])
+    x64 = x.double()
+    want = shape.scale * ((torch.nn.functional.silu(x64 @ wg64.T) * (x64 @ wu64.T)) @ wd64.T)
+    np.testing.assert_allclose(out, want.numpy(), rtol=1e-10, atol=1e-12)
+
 ALL_CHECKS = [
     check_golden_cases, check_invariants, check_sigmoid_and_bias, check_group_scores_vs_topk,
     check_group_choice_brute_force, check_selection_brute_force_small, check_plain_topk_reduction,
@@ -380,4 +452,5 @@ ALL_CHECKS = [
     check_identical_experts, check_given_selection,
     pin_rmsnorm_library, pin_rmsnorm_closed_forms, pin_residual_is_scaled_sum, pin_round_bf16_vs_torch,
     pin_sublayer_composition, pin_e4m3_decoder_vs_torch, pin_fp8_expert_vs_torch, pin_forward_grouped_vs_per_token,
+    pin_forward_fp8_equals_bf16_block, pin_forward_fp8_identical_experts,
 ]

@@ -1,5 +1,11 @@
 """The pins are strong enough: each plausible mistake planted in a copy of the oracle
-(on the CPU) must make at least one pin fail. The real oracle is never modified."""
+(on the CPU) must make at least one pin fail. The real oracle is never modified: C
+mistakes go into a recompiled copy of its source, Python mistakes into a re-defined copy
+of one method bound to a single oracle instance."""
+import inspect
+import textwrap
+import types
+
 import pytest
 
 import pins
@@ -50,6 +56,36 @@ def test_mutant_is_caught(name, old, new):
     src = open(O.SRC).read()
     assert src.count(old) == 1, f"mutation anchor for {name} must occur once"
     orc = O.Oracle(O.build_variant(src.replace(old, new), name))
+    caught = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except (AssertionError, RuntimeError) as exc:  # noqa: PERF203
+            caught.append((check.__name__, type(exc).__name__))
+            break
+    assert caught, f"no pin catches the planted mistake {name}"
+
+
+# Mistakes in the Python compositions of the oracle: (name, method, text, replacement).
+PY_MUTANTS = [
+    ("fp8_weights_from_biased_score", "forward_fp8", 's = dbg["s"].astype(np.float64)',
+     's = dbg["c"].astype(np.float64)'),
+    ("fp8_given_weights_scale_missing", "forward_fp8", "w64 = shape.scale * picked / picked.sum(axis=1, keepdims=True)",
+     "w64 = picked / picked.sum(axis=1, keepdims=True)"),
+    ("fp8_combine_drops_slot", "forward_fp8", "for k in range(shape.top_k):",
+     "for k in range(shape.top_k - 1):"),
+    ("fp8_weights_not_normalised", "forward_fp8", "w64 = dbg[\"w64\"]", "w64 = dbg[\"w64\"] * 1.001"),
+]
+
+
+@pytest.mark.parametrize("name,method,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_python_mutant_is_caught(name, method, old, new):
+    src = textwrap.dedent(inspect.getsource(getattr(O.Oracle, method)))
+    assert src.count(old) == 1, f"mutation anchor for {name} must occur once"
+    namespace = dict(vars(O))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), namespace)  # noqa: S102
+    orc = O.Oracle(O.build())
+    setattr(orc, method, types.MethodType(namespace[method], orc))
     caught = []
     for check in pins.ALL_CHECKS:
         try:
