@@ -25,7 +25,8 @@
  *     a call returns. Outputs must not alias inputs.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream): results are valid
  *     once the stream has synchronised. No entry point synchronises the host except
- *     beam_moe_device_status and beam_moe_timing_read.
+ *     beam_moe_forward_host, beam_moe_device_status, beam_moe_route_noalloc_status and
+ *     beam_moe_timing_read.
  *   - Scratch memory is taken from a library-owned stream-ordered pool on the current
  *     device and returned before the call's work completes (cudaMallocFromPoolAsync /
  *     cudaFreeAsync on `stream`); the pool keeps freed memory cached for the next call.
@@ -110,6 +111,17 @@ BEAM_MOE_API int beam_moe_forward_ex(const beam_moe_config *cfg, const __nv_bflo
                         const float *expert_bias, const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up,
                         const __nv_bfloat16 *w_down, int T, __nv_bfloat16 *out, cudaStream_t stream);
 
+/* The block of beam_moe_forward_ex with the tokens and the output in HOST memory: copies
+ * x_host [T, d] BF16 to the device, runs the block, copies the output back to out_host
+ * [T, d] BF16, all on `stream`, and returns once the stream has finished (this call
+ * synchronises the host). The device copies of x and out come from the library's pool.
+ * Page-locked (pinned) host buffers let the copies run asynchronously; pageable ones work,
+ * with copies the driver stages. The weights, router and bias are device pointers as for
+ * beam_moe_forward_ex; errors as there. */
+BEAM_MOE_API int beam_moe_forward_host(const beam_moe_config *cfg, const __nv_bfloat16 *x_host, const float *router_w,
+                          const float *expert_bias, const __nv_bfloat16 *w_gate, const __nv_bfloat16 *w_up,
+                          const __nv_bfloat16 *w_down, int T, __nv_bfloat16 *out_host, cudaStream_t stream);
+
 /* Whole MoE block with FP8 expert weights. The pages ship FP8 (and NVFP4) checkpoints of the
  * model (Glonce "Reflection releases Beam ...", Hardware paragraph; transformers "Beam" doc,
  * checkpoint formats) but give no quantisation recipe; this call takes the plainest
@@ -191,21 +203,49 @@ BEAM_MOE_API int beam_moe_sublayer_forward(const beam_moe_config *cfg, const __n
  * deployment variant of beam_moe_route_ex for callers that must not have a library
  * allocate device memory (an engine that has claimed all free HBM for weights and KV
  * cache, or a per-token path where an allocator call could synchronise the device or
- * stall). Same arguments, layouts and results as beam_moe_route_ex; calls no cudaMalloc,
+ * stall). Same arguments, layouts and outputs as beam_moe_route_ex; calls no cudaMalloc,
  * cudaFree or pool allocation.
  *   - Scratch: one fixed array of BEAM_MOE_NOALLOC_SCRATCH_BYTES in the library's device
  *     image; every GPU that loads the library holds it until the process exits.
  *   - Limit: T <= BEAM_MOE_NOALLOC_MAX_TOKENS, else BEAM_MOE_ERR_ARG with a message.
+ *   - Results equal beam_moe_route_ex's bit for bit while the array holds the K split
+ *     count beam_moe_route_ex picks, which is the case for every T <= 8192 on a 148-SM
+ *     B300 at Beam's shape. On a GPU where it cannot (more SMs, hence more splits), fewer
+ *     splits are used: only the summation order of the FP32 logits differs then, which can
+ *     change a pick only between near-tied experts. beam_moe_route_noalloc_plan tells.
  *   - The first call on each device looks up the array's device address (with that device
  *     current); make that first call before any stream capture.
  *   - All calls share the array and it keeps the last call's contents (every value a call
  *     reads is written earlier in the same call). Calls that overlap on the GPU race on
  *     it: serialise them (one stream, or events between streams).
+ *   - Kernel errors (a pipeline wait that ran past its limit) go to this entry point's own
+ *     status word, read with beam_moe_route_noalloc_status, not beam_moe_device_status.
  *   - Not counted by beam_moe_last_launch_count or timed by beam_moe_timing_*. */
 #define BEAM_MOE_NOALLOC_MAX_TOKENS 8192
 #define BEAM_MOE_NOALLOC_SCRATCH_BYTES (40u << 20)
 BEAM_MOE_API int beam_moe_route_noalloc(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
                            const float *expert_bias, int T, int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+
+/* Host-only planning query of beam_moe_route_noalloc (no GPU work, no allocation): writes to
+ * *splits the number of K split planes a call with T tokens makes on a GPU with num_sms SMs,
+ * or returns BEAM_MOE_ERR_ARG if T is outside [1, BEAM_MOE_NOALLOC_MAX_TOKENS] or the array
+ * cannot hold even one plane. The split count of beam_moe_route_ex is the same unless the
+ * array forced fewer. */
+BEAM_MOE_API int beam_moe_route_noalloc_plan(const beam_moe_config *cfg, int T, int num_sms, int *splits);
+
+/* Synchronises `stream`, then returns and clears the no-allocation router's kernel status
+ * word on the current device: BEAM_MOE_OK, or BEAM_MOE_ERR_DEVICE if one of its kernels
+ * recorded an error since the last read (its outputs are then not valid). Allocates
+ * nothing. */
+BEAM_MOE_API int beam_moe_route_noalloc_status(cudaStream_t stream);
+
+/* Self-test of the no-allocation router's failure detection (no counterpart on the pages):
+ * runs its tensor-core logits kernel on one tile of zeros laid out in the fixed array, with
+ * the first pipeline stage expecting 16 bytes more than its copies deliver, so the MMA
+ * thread's bounded wait (2 s) runs out and the kernel records it in the status word that
+ * beam_moe_route_noalloc_status reads; the CTA frees its tensor memory and exits, and the
+ * context stays usable. Overwrites the start of the array; allocates nothing. */
+BEAM_MOE_API int beam_moe_route_noalloc_selftest(cudaStream_t stream);
 
 /* Router logits only (output_router_logits in the transformers doc, Notes): the same
  * kernels as the router's first stage; logits fp32 [T, E]. */
@@ -244,6 +284,14 @@ BEAM_MOE_API int beam_moe_timing_read(float *ms, int max_stages);
 
 /* Number of kernel launches the last forward/route call on this thread made. */
 BEAM_MOE_API int beam_moe_last_launch_count(void);
+
+/* Debug aid (process-wide): while enabled, every scratch allocation of the pool-backed
+ * entry points is filled with 0xFF bytes (NaN in BF16 and FP32, -1 in int32) on `stream`
+ * before the call's kernels run, so that any scratch value read before it is written
+ * reaches the output as a NaN or an out-of-range index (recorded in the status word). The
+ * results of a correct build do not change. Off by default; the environment variable
+ * BEAM_MOE_DEBUG=1 turns it on at the library's first call. Costs one memset per call. */
+BEAM_MOE_API int beam_moe_debug_poison_scratch(int enable);
 
 #ifdef __cplusplus
 }

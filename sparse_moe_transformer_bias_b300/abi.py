@@ -32,7 +32,9 @@ EXPORTS = ("beam_moe_default_config", "beam_moe_route", "beam_moe_route_ex", "be
            "beam_moe_forward_ex", "beam_moe_router_logits", "beam_moe_last_error", "beam_moe_device_status",
            "beam_moe_timing_enable", "beam_moe_timing_read", "beam_moe_last_launch_count",
            "beam_moe_route_noalloc", "beam_moe_rmsnorm", "beam_moe_sublayer_forward", "beam_moe_forward_shard",
-           "beam_moe_dense_mlp", "beam_moe_forward_fp8", "beam_moe_selftest_wait_timeout")
+           "beam_moe_dense_mlp", "beam_moe_forward_fp8", "beam_moe_selftest_wait_timeout",
+           "beam_moe_route_noalloc_plan", "beam_moe_route_noalloc_status", "beam_moe_route_noalloc_selftest",
+           "beam_moe_forward_host", "beam_moe_debug_poison_scratch")
 
 
 class BeamMoeConfig(ctypes.Structure):
@@ -72,7 +74,11 @@ def load() -> ctypes.CDLL:
             L.beam_moe_forward.argtypes = [P, P, P, P, P, P, i, P, P]
             L.beam_moe_forward_ex.argtypes = [cfgp, P, P, P, P, P, P, i, P, P]
             L.beam_moe_router_logits.argtypes = [cfgp, P, P, i, P, P]
+            L.beam_moe_forward_host.argtypes = [cfgp, P, P, P, P, P, P, i, P, P]
             L.beam_moe_route_noalloc.argtypes = [cfgp, P, P, P, i, P, P, P]
+            L.beam_moe_route_noalloc_plan.argtypes = [cfgp, i, i, ctypes.POINTER(ctypes.c_int)]
+            L.beam_moe_route_noalloc_status.argtypes = [P]
+            L.beam_moe_route_noalloc_selftest.argtypes = [P]
             f32 = ctypes.c_float
             L.beam_moe_rmsnorm.argtypes = [i, P, P, f32, i, P, P]
             L.beam_moe_sublayer_forward.argtypes = [cfgp, P, P, P, f32, i, P, P, P, P, P, i, P, P]
@@ -86,11 +92,14 @@ def load() -> ctypes.CDLL:
             L.beam_moe_timing_enable.argtypes = [i]
             L.beam_moe_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), i]
             L.beam_moe_last_launch_count.argtypes = []
+            L.beam_moe_debug_poison_scratch.argtypes = [i]
             for f in ("beam_moe_route", "beam_moe_route_ex", "beam_moe_forward", "beam_moe_forward_ex",
                       "beam_moe_router_logits", "beam_moe_device_status", "beam_moe_timing_enable",
                       "beam_moe_timing_read", "beam_moe_last_launch_count", "beam_moe_route_noalloc",
                       "beam_moe_rmsnorm", "beam_moe_sublayer_forward", "beam_moe_forward_shard",
-                      "beam_moe_dense_mlp", "beam_moe_forward_fp8", "beam_moe_selftest_wait_timeout"):
+                      "beam_moe_dense_mlp", "beam_moe_forward_fp8", "beam_moe_selftest_wait_timeout",
+           "beam_moe_route_noalloc_plan", "beam_moe_route_noalloc_status", "beam_moe_route_noalloc_selftest",
+           "beam_moe_forward_host", "beam_moe_debug_poison_scratch"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -149,11 +158,38 @@ def beam_moe_forward_ex(cfg, x, router_w, expert_bias, w_gate, w_up, w_down, T, 
                                              _ptr(w_up), _ptr(w_down), int(T), _ptr(out), _stream(stream)))
 
 
+def beam_moe_forward_host(cfg, x_host, router_w, expert_bias, w_gate, w_up, w_down, T, out_host, stream=None):
+    """The block with x and out in host memory (pinned for asynchronous copies); returns once
+    the stream has finished."""
+    return _check(load().beam_moe_forward_host(_cfg(cfg), _ptr(x_host), _ptr(router_w), _ptr(expert_bias),
+                                               _ptr(w_gate), _ptr(w_up), _ptr(w_down), int(T), _ptr(out_host),
+                                               _stream(stream)))
+
+
 def beam_moe_route_noalloc(cfg, x, router_w, expert_bias, T, topk_idx, topk_w, stream=None):
     """beam_moe_route_ex without any device allocation (fixed scratch array in the
     library; T <= BEAM_MOE_NOALLOC_MAX_TOKENS)."""
     return _check(load().beam_moe_route_noalloc(_cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), int(T),
                                                 _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
+def beam_moe_route_noalloc_plan(cfg, T, num_sms) -> int:
+    """K split planes a no-allocation router call with T tokens makes on a GPU with num_sms
+    SMs (host-only query; raises if the batch does not fit the fixed array)."""
+    n = ctypes.c_int(0)
+    _check(load().beam_moe_route_noalloc_plan(_cfg(cfg), int(T), int(num_sms), ctypes.byref(n)))
+    return n.value
+
+
+def beam_moe_route_noalloc_status(stream=None):
+    """Raise if a kernel of the no-allocation router recorded an error (read and clear)."""
+    return _check(load().beam_moe_route_noalloc_status(_stream(stream)))
+
+
+def beam_moe_route_noalloc_selftest(stream=None):
+    """Queue the no-allocation router's failure-detection self-test (a bounded wait that
+    runs out); read the outcome with beam_moe_route_noalloc_status()."""
+    return _check(load().beam_moe_route_noalloc_selftest(_stream(stream)))
 
 
 def beam_moe_forward_shard(cfg, x, router_w, expert_bias, w_gate, w_up, w_down, e_begin, e_end, T, out_partial,
@@ -217,6 +253,11 @@ def beam_moe_timing_read() -> dict:
     if n < 0:
         _check(n)
     return {name: float(buf[i]) for i, name in enumerate(STAGES)}
+
+
+def beam_moe_debug_poison_scratch(enable: bool):
+    """Fill every scratch allocation with NaN bytes before use (debug aid, process-wide)."""
+    return _check(load().beam_moe_debug_poison_scratch(1 if enable else 0))
 
 
 def beam_moe_last_launch_count() -> int:

@@ -1,9 +1,11 @@
 // C ABI of libbeam_moe.so (declared and documented in include/beam_moe.h): argument
 // checks, per-device state (scratch pool, status word), scratch layout and the launch
 // sequence of the Beam MoE forward pass.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -15,6 +17,28 @@ namespace {
 
 thread_local char g_err[512] = "";
 thread_local int g_launches = 0;
+
+// Debug aid: fill every scratch allocation with 0xFF bytes (NaN in BF16 and FP32, -1 in
+// int32) before the call's kernels run, so that a value read before it is written shows
+// up in the output. Off unless beam_moe_debug_poison_scratch(1) or BEAM_MOE_DEBUG=1.
+std::atomic<int> g_poison{-1};  // -1: not yet read from the environment
+
+bool poison_scratch() {
+    int v = g_poison.load(std::memory_order_relaxed);
+    if (v < 0) {
+        const char* env = getenv("BEAM_MOE_DEBUG");
+        v = (env && env[0] && strcmp(env, "0") != 0) ? 1 : 0;
+        int expect = -1;
+        g_poison.compare_exchange_strong(expect, v);
+        v = g_poison.load(std::memory_order_relaxed);
+    }
+    return v == 1;
+}
+
+// Fills a fresh scratch allocation when the debug aid is on.
+cudaError_t maybe_poison(void* mem, size_t bytes, cudaStream_t st) {
+    return poison_scratch() ? cudaMemsetAsync(mem, 0xFF, bytes, st) : cudaSuccess;
+}
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -299,6 +323,10 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, st);
     if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "scratch allocation of %zu bytes: %s", bytes, cudaGetErrorString(e));
     layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, static_cast<char*>(mem), &sc);
+    if ((e = maybe_poison(mem, bytes, st)) != cudaSuccess) {
+        rc = fail(BEAM_MOE_ERR_CUDA, "scratch poison: %s", cudaGetErrorString(e));
+        goto done;
+    }
     {
         int32_t* idx = mode == 0 ? topk_idx : sc.idx;
         float* w = mode == 0 ? topk_w : sc.w;
@@ -406,6 +434,43 @@ int beam_moe_forward(const __nv_bfloat16* x, const float* router_w, const float*
     return beam_moe_forward_ex(&c, x, router_w, expert_bias, w_gate, w_up, w_down, T, out, stream);
 }
 
+int beam_moe_forward_host(const beam_moe_config* cfg, const __nv_bfloat16* x_host, const float* router_w,
+                          const float* expert_bias, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,
+                          const __nv_bfloat16* w_down, int T, __nv_bfloat16* out_host, cudaStream_t stream) {
+    int rc;
+    if ((rc = check_cfg(cfg)) || (rc = check_T(T))) return rc;
+    if (!x_host) return fail(BEAM_MOE_ERR_ARG, "x_host is null");
+    if (!out_host) return fail(BEAM_MOE_ERR_ARG, "out_host is null");
+    if (T == 0) return BEAM_MOE_OK;
+    if ((rc = check_stream(stream))) return rc;
+    DeviceState* dev = nullptr;
+    if ((rc = device_state(&dev))) return rc;
+    const size_t row_bytes = static_cast<size_t>(cfg->d) * sizeof(bf16);
+    const size_t bytes = ((static_cast<size_t>(T) * row_bytes + 255) & ~size_t(255)) * 2;
+    void* mem = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, stream);
+    if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "device buffers of %zu bytes: %s", bytes, cudaGetErrorString(e));
+    bf16* x_dev = static_cast<bf16*>(mem);
+    bf16* out_dev = reinterpret_cast<bf16*>(static_cast<char*>(mem) + bytes / 2);
+    rc = BEAM_MOE_OK;
+    if ((e = cudaMemcpyAsync(x_dev, x_host, T * row_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        rc = fail(BEAM_MOE_ERR_CUDA, "copy of x to the device: %s", cudaGetErrorString(e));
+    if (rc == BEAM_MOE_OK)
+        rc = run(cfg, x_dev, router_w, expert_bias, w_gate, w_up, w_down, T, nullptr, nullptr, nullptr, out_dev, 2,
+                 stream);
+    const int launches = g_launches;
+    if (rc == BEAM_MOE_OK &&
+        (e = cudaMemcpyAsync(out_host, out_dev, T * row_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        rc = fail(BEAM_MOE_ERR_CUDA, "copy of out to the host: %s", cudaGetErrorString(e));
+    e = cudaFreeAsync(mem, stream);
+    if (rc == BEAM_MOE_OK && e != cudaSuccess) rc = fail(BEAM_MOE_ERR_CUDA, "buffer release: %s", cudaGetErrorString(e));
+    e = cudaStreamSynchronize(stream);
+    if (rc == BEAM_MOE_OK && e != cudaSuccess)
+        rc = fail(BEAM_MOE_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    g_launches = launches;
+    return rc;
+}
+
 int beam_moe_sublayer_forward(const beam_moe_config* cfg, const __nv_bfloat16* stream_in,
                               const __nv_bfloat16* pre_gamma, const __nv_bfloat16* post_gamma, float eps, int k,
                               const float* router_w, const float* expert_bias, const __nv_bfloat16* w_gate,
@@ -465,6 +530,10 @@ int beam_moe_dense_mlp(int d, int I, const __nv_bfloat16* x, const __nv_bfloat16
     bf16* h = cc.take<bf16>(static_cast<size_t>(T) * I);
     const cudaStream_t st = stream;
     rc = BEAM_MOE_OK;
+    if ((e = maybe_poison(mem, bytes, st)) != cudaSuccess) {
+        rc = fail(BEAM_MOE_ERR_CUDA, "scratch poison: %s", cudaGetErrorString(e));
+        goto done;
+    }
     LAUNCH(kCount, launch_dense_tiles(T, bn_max, tiles, tile_done, st));
     LAUNCH(kExpert, launch_expert_mlp(s, w_gate, w_up, w_down, x, T, tiles, tile_done, max_tiles, bn_max, h, out,
                                       dev->status, dev->num_sms, st));
@@ -586,5 +655,10 @@ int beam_moe_timing_read(float* ms, int max_stages) {
 }
 
 int beam_moe_last_launch_count(void) { return g_launches; }
+
+int beam_moe_debug_poison_scratch(int enable) {
+    g_poison.store(enable ? 1 : 0, std::memory_order_relaxed);
+    return BEAM_MOE_OK;
+}
 
 }  // extern "C"

@@ -662,7 +662,7 @@ cudaError_t launch_mlp(const CUtensorMap& wg, const CUtensorMap& wu, const CUten
                        const BMaps& h, const MlpArgs& args, int grid, cudaStream_t st) {
     using C = MlpCfg<kBNMax, kFP8>;
     auto kern = expert_mlp_kernel<kBNMax, kFP8>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = set_smem_limit_once<expert_mlp_kernel<kBNMax, kFP8>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const cudaError_t le_ =
         launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, wg, wu, wd, x, h, args);

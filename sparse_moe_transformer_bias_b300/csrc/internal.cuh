@@ -1,5 +1,6 @@
 // Declarations shared by the kernels' host launchers and the C-ABI layer.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -37,6 +38,22 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cfg.numAttrs = 1;
 #endif
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// Raises kernel Kern's dynamic shared-memory limit to `bytes` once per device (the setting
+// lasts for the device's context), so steady-state launches make no attribute call. One
+// instantiation per kernel: the flag word belongs to that kernel alone.
+template <auto Kern>
+cudaError_t set_smem_limit_once(int bytes) {
+    static std::atomic<uint64_t> done{0};  // bit d: set on device d (devices 0..63)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
 }
 
 struct Shape {
@@ -126,8 +143,11 @@ cudaError_t launch_dense_tiles(int T, int bn_max, int4* tiles, int* tile_done, c
 // Split-K count of the tensor-core router product for T tokens.
 int router_tc_splits(const Shape& s, int T, int num_sms);
 // partial[split][t][e] = sum over the split's K range of x[t] . (hi + mid + lo)[e].
+// selftest_extra_tx > 0 (failure-detection self-test only): the first pipeline stage of CTA
+// 0 expects that many bytes more than its copies bring, so the MMA thread's bounded wait on
+// it runs out and the kernel records kStatusWaitTimeout in `status`.
 cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int T, int splits, float* partial,
-                             int* status, int num_sms, cudaStream_t st);
+                             int* status, int num_sms, cudaStream_t st, uint32_t selftest_extra_tx = 0);
 
 // ---------------------------------------------------------------- combine (combine.cu)
 cudaError_t launch_combine(const Shape& s, const bf16* y, const int* inv_slot, const float* topk_w, int T, bf16* out,

@@ -15,7 +15,13 @@
 // or not this entry point is ever called. It fits the router scratch of any call with
 // T <= BEAM_MOE_NOALLOC_MAX_TOKENS (8192) at Beam's shape on GPUs of up to ~170 SMs. On a
 // GPU where the router would pick more K splits than the array holds, fewer splits are
-// used; only the summation order of the logits changes then.
+// used; only the summation order of the logits changes then (noalloc_plan below; the
+// exported beam_moe_route_noalloc_plan gives the same answer for any SM count).
+//
+// A second file-scope word holds this entry point's kernel status: the tensor-core logits
+// kernel records there a pipeline wait that ran past its limit (its partial planes are then
+// incomplete, and the array still holds the previous call's values), and
+// beam_moe_route_noalloc_status reads and clears it without touching the library's pool.
 //
 // Host code cannot pass the array's name to a kernel (on the host it is a stand-in
 // symbol, not a device address), so the first call on each device looks up the array's
@@ -31,6 +37,7 @@
 #include "internal.cuh"
 
 static __device__ __align__(256) uint8_t g_route_noalloc_scratch[BEAM_MOE_NOALLOC_SCRATCH_BYTES];
+static __device__ int g_route_noalloc_status;  // 0, or the first status code a kernel recorded
 
 namespace beam {
 namespace {
@@ -39,6 +46,7 @@ struct NoAllocDevice {
     bool ready = false;
     int num_sms = 0;
     uint8_t* scratch = nullptr;  // device address of g_route_noalloc_scratch on this device
+    int* status = nullptr;       // device address of g_route_noalloc_status on this device
 };
 constexpr int kMaxNoAllocDevices = 64;
 NoAllocDevice g_noalloc[kMaxNoAllocDevices];
@@ -59,16 +67,101 @@ int noalloc_device(NoAllocDevice** out) {
         if ((e = cudaGetSymbolAddress(&p, g_route_noalloc_scratch)) != cudaSuccess || p == nullptr)
             return abi_fail(BEAM_MOE_ERR_CUDA, "cudaGetSymbolAddress(router scratch): %s", cudaGetErrorString(e));
         s.scratch = static_cast<uint8_t*>(p);
+        p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_route_noalloc_status)) != cudaSuccess || p == nullptr)
+            return abi_fail(BEAM_MOE_ERR_CUDA, "cudaGetSymbolAddress(router status): %s", cudaGetErrorString(e));
+        s.status = static_cast<int*>(p);
         s.ready = true;
     }
     *out = &s;
     return BEAM_MOE_OK;
 }
 
+// The router plan of a call with T tokens on a GPU with num_sms SMs, its K split count
+// lowered (to divisors of the d/64 K chunks) until the BF16 weight pieces and the FP32
+// partial planes fit the array. Returns BEAM_MOE_OK, or BEAM_MOE_ERR_ARG with a message if
+// T is outside [1, BEAM_MOE_NOALLOC_MAX_TOKENS] or even one split does not fit.
+int noalloc_plan(const Shape& s, int T, int num_sms, RouterPlan* plan, size_t* w3_bytes) {
+    if (T < 1 || T > BEAM_MOE_NOALLOC_MAX_TOKENS)
+        return abi_fail(BEAM_MOE_ERR_ARG,
+                        "T=%d is outside [0, %d], the token limit of beam_moe_route_noalloc (its fixed scratch "
+                        "array holds %u bytes); use beam_moe_route_ex for larger batches",
+                        T, BEAM_MOE_NOALLOC_MAX_TOKENS, static_cast<unsigned>(BEAM_MOE_NOALLOC_SCRATCH_BYTES));
+    if (num_sms < 1) return abi_fail(BEAM_MOE_ERR_ARG, "num_sms=%d must be positive", num_sms);
+    RouterPlan p = router_plan(s, T, num_sms);
+    const size_t wb = (p.w3_elems * sizeof(bf16) + 255) & ~size_t(255);
+    const size_t capacity = BEAM_MOE_NOALLOC_SCRATCH_BYTES;
+    const size_t plane = static_cast<size_t>(T) * s.E * sizeof(float);
+    const int nk = s.d / 64;  // K chunks of the tensor-core product; its splits divide it
+    while (p.splits > 1 && wb + static_cast<size_t>(p.splits) * plane > capacity) {
+        do {
+            --p.splits;
+        } while (nk % p.splits);
+    }
+    if (wb + static_cast<size_t>(p.splits) * plane > capacity)
+        return abi_fail(BEAM_MOE_ERR_ARG, "T=%d with E=%d and d=%d needs more router scratch than the %u bytes of "
+                        "beam_moe_route_noalloc", T, s.E, s.d, static_cast<unsigned>(capacity));
+    *plan = p;
+    *w3_bytes = wb;
+    return BEAM_MOE_OK;
+}
+
+Shape shape_of_cfg(const beam_moe_config* c) {
+    return Shape{c->d, c->I, c->E, c->n_group, c->topk_group, c->top_k, c->scale};
+}
+
 }  // namespace
 }  // namespace beam
 
 using namespace beam;
+
+extern "C" int beam_moe_route_noalloc_plan(const beam_moe_config* cfg, int T, int num_sms, int* splits) {
+    int rc;
+    if ((rc = abi_check_config(cfg))) return rc;
+    if (!splits) return abi_fail(BEAM_MOE_ERR_ARG, "splits is null");
+    RouterPlan plan;
+    size_t w3_bytes = 0;
+    if ((rc = noalloc_plan(shape_of_cfg(cfg), T, num_sms, &plan, &w3_bytes))) return rc;
+    *splits = plan.splits;
+    return BEAM_MOE_OK;
+}
+
+extern "C" int beam_moe_route_noalloc_status(cudaStream_t stream) {
+    int rc;
+    if ((rc = abi_check_stream(stream))) return rc;
+    NoAllocDevice* dev = nullptr;
+    if ((rc = noalloc_device(&dev))) return rc;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return abi_fail(BEAM_MOE_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    int word = 0;
+    if ((e = cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return abi_fail(BEAM_MOE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (word == kStatusOk) return BEAM_MOE_OK;
+    if ((e = cudaMemset(dev->status, 0, sizeof word)) != cudaSuccess)
+        return abi_fail(BEAM_MOE_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+    return abi_fail(BEAM_MOE_ERR_DEVICE, "no-allocation router kernel status %d (%s)", word,
+                    word == kStatusWaitTimeout ? "a GEMM pipeline wait ran past its limit" : "unknown");
+}
+
+extern "C" int beam_moe_route_noalloc_selftest(cudaStream_t stream) {
+    int rc;
+    if ((rc = abi_check_stream(stream))) return rc;
+    NoAllocDevice* dev = nullptr;
+    if ((rc = noalloc_device(&dev))) return rc;
+    // One 128-expert tile of the tensor-core logits product over d = 128, 48 tokens, on
+    // zeros laid out in the array: weight pieces [3][128][128], tokens [48][128], one plane.
+    const Shape s{128, 128, 128, 4, 1, 1, 1.0f};
+    const int T = 48;
+    bf16* w3 = reinterpret_cast<bf16*>(dev->scratch);
+    bf16* x = w3 + 3 * 128 * 128;
+    float* partial = reinterpret_cast<float*>(x + T * 128);
+    const size_t bytes = reinterpret_cast<uint8_t*>(partial + T * 128) - dev->scratch;
+    cudaError_t e = cudaMemsetAsync(dev->scratch, 0, bytes, stream);
+    if (e != cudaSuccess) return abi_fail(BEAM_MOE_ERR_CUDA, "scratch clear: %s", cudaGetErrorString(e));
+    e = launch_router_tc(s, w3, x, T, 1, partial, dev->status, 1, stream, 16u);
+    if (e != cudaSuccess) return abi_fail(BEAM_MOE_ERR_CUDA, "launch of router logits failed: %s", cudaGetErrorString(e));
+    return BEAM_MOE_OK;
+}
 
 extern "C" int beam_moe_route_noalloc(const beam_moe_config* cfg, const __nv_bfloat16* x, const float* router_w,
                                       const float* expert_bias, int T, int32_t* topk_idx, float* topk_w,
@@ -89,20 +182,12 @@ extern "C" int beam_moe_route_noalloc(const beam_moe_config* cfg, const __nv_bfl
     NoAllocDevice* dev = nullptr;
     if ((rc = noalloc_device(&dev))) return rc;
 
-    const Shape s{cfg->d, cfg->I, cfg->E, cfg->n_group, cfg->topk_group, cfg->top_k, cfg->scale};
-    // Same plan as beam_moe_route_ex; layout: weight pieces, then the partial planes.
-    RouterPlan plan = router_plan(s, T, dev->num_sms);
-    const size_t w3_bytes = (plan.w3_elems * sizeof(bf16) + 255) & ~size_t(255);
-    const size_t capacity = sizeof(g_route_noalloc_scratch);
-    const int nk = s.d / 64;  // K chunks of the tensor-core product; its splits divide it
-    while (plan.splits > 1 && w3_bytes + static_cast<size_t>(plan.splits) * T * s.E * sizeof(float) > capacity) {
-        do {
-            --plan.splits;
-        } while (nk % plan.splits);
-    }
-    if (w3_bytes + static_cast<size_t>(plan.splits) * T * s.E * sizeof(float) > capacity)
-        return abi_fail(BEAM_MOE_ERR_ARG, "T=%d with E=%d and d=%d needs more router scratch than the %u bytes of "
-                        "beam_moe_route_noalloc", T, s.E, s.d, static_cast<unsigned>(capacity));
+    const Shape s = shape_of_cfg(cfg);
+    // Same plan as beam_moe_route_ex (fewer splits only if the array cannot hold them);
+    // layout: weight pieces, then the partial planes.
+    RouterPlan plan;
+    size_t w3_bytes = 0;
+    if ((rc = noalloc_plan(s, T, dev->num_sms, &plan, &w3_bytes))) return rc;
     bf16* w3 = plan.tensor ? reinterpret_cast<bf16*>(dev->scratch) : nullptr;
     float* partial = reinterpret_cast<float*>(dev->scratch + w3_bytes);
     cudaError_t e = cudaSuccess;
@@ -111,7 +196,7 @@ extern "C" int beam_moe_route_noalloc(const beam_moe_config* cfg, const __nv_bfl
         if (e != cudaSuccess)
             return abi_fail(BEAM_MOE_ERR_CUDA, "launch of router weight split failed: %s", cudaGetErrorString(e));
     }
-    e = launch_router_logits(s, plan, x, router_w, T, w3, partial, nullptr, dev->num_sms, stream);
+    e = launch_router_logits(s, plan, x, router_w, T, w3, partial, dev->status, dev->num_sms, stream);
     if (e != cudaSuccess) return abi_fail(BEAM_MOE_ERR_CUDA, "launch of router logits failed: %s", cudaGetErrorString(e));
     e = launch_router_select(s, partial, plan.splits, expert_bias, T, topk_idx, topk_w, nullptr, stream);
     if (e != cudaSuccess) return abi_fail(BEAM_MOE_ERR_CUDA, "launch of router select failed: %s", cudaGetErrorString(e));

@@ -55,6 +55,8 @@ struct RouterArgs {
     int k_chunks;        // 64-wide K chunks per range
     float* partial;      // [splits][T][E]
     int* status;         // may be null
+    uint32_t extra_tx;   // self-test only (0 otherwise): bytes the first stage of CTA 0 expects
+                         // beyond what its copies deliver, so that stage never completes
 };
 
 struct Item {
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued = 0, parity = 0;  // per stage: ever loaded / parity of the last load
             bool ok = true;
+            uint32_t extra = blockIdx.x == 0 ? args.extra_tx : 0u;
             for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
                 const Item it = item_of(args, item);
                 const int b_rows = ((it.rows + kBoxRows - 1) / kBoxRows) * kBoxRows;
@@ -145,7 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t sa = ptx::smem_u32(smem + stage * C::kStage);
-                    ptx::mbar_arrive_expect_tx(bar(FULL0 + stage), bytes);
+                    ptx::mbar_arrive_expect_tx(bar(FULL0 + stage), bytes + extra);
+                    extra = 0u;
 #pragma unroll
                     for (int j = 0; j < kPieces; ++j)
                         ptx::tma_load_2d(sa + j * C::kA, &tmW, kx, j * args.E + it.m * kTileM, bar(FULL0 + stage),
@@ -295,7 +299,7 @@ int router_tc_splits(const Shape& s, int T, int num_sms) {
 }
 
 cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int T, int splits, float* partial,
-                             int* status, int num_sms, cudaStream_t st) {
+                             int* status, int num_sms, cudaStream_t st, uint32_t selftest_extra_tx) {
     CUtensorMap w;
     BMaps b;
     const char* why = nullptr;
@@ -311,10 +315,10 @@ cudaError_t launch_router_tc(const Shape& s, const bf16* w3, const bf16* x, int 
     a.k_chunks = kc_total / splits;
     a.partial = partial;
     a.status = status;
+    a.extra_tx = selftest_extra_tx;
     const long long items = static_cast<long long>((T + kBN - 1) / kBN) * a.m_tiles * splits;
     const int grid = static_cast<int>(items < num_sms ? (items < 1 ? 1 : items) : num_sms);
-    cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::kSmemBytes);
+    cudaError_t e = set_smem_limit_once<router_gemm_kernel>(Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     const cudaError_t le_ = launch_pdl(router_gemm_kernel, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, st, w, b, a);
     if (le_ != cudaSuccess) return le_;

@@ -3,7 +3,7 @@
     out = moe.forward(x, router_w, bias, w_gate, w_up, w_down)          # Beam shape
     idx, w = moe.route(x, router_w, bias, shape=workloads.TINY)
     logits = moe.router_logits(x, router_w)
-    out = moe.forward_host(x_pinned, ...)     # host in, host out (copies on the stream)
+    out = moe.forward_host(x_pinned, ...)     # host in, host out, one library call
     part = moe.forward_shard(x, router_w, bias, wg[lo:hi], wu[lo:hi], wd[lo:hi], lo, hi)  # FP32
     x = moe.rmsnorm(stream, gamma, eps)
     new_stream = moe.sublayer_forward(stream, pre_gamma, post_gamma, eps, k, router_w, bias, w_gate, w_up, w_down)
@@ -68,24 +68,19 @@ def forward_fp8(x, router_w, bias, experts_fp8, shape: MoEShape = BEAM, out=None
     return out
 
 
-def forward_host(x_host, router_w, bias, w_gate, w_up, w_down, shape: MoEShape = BEAM, x_dev=None, out_dev=None,
-                 out_host=None, stream=None):
-    """Host tokens in, host output out: copies x to the device, runs the block, copies
-    the output back, all on `stream`; returns out_host once the stream has finished."""
-    stream = stream or torch.cuda.current_stream()
+def forward_host(x_host, router_w, bias, w_gate, w_up, w_down, shape: MoEShape = BEAM, out_host=None, stream=None):
+    """Host tokens in, host output out, in one library call (beam_moe_forward_host): the copy
+    of x to the device, the block and the copy of the output back, on `stream`; returns
+    out_host once the stream has finished. Pinned host tensors keep the copies asynchronous."""
     T = x_host.shape[0]
-    dev = router_w.device
-    if x_dev is None:
-        x_dev = torch.empty((T, shape.d), dtype=torch.bfloat16, device=dev)
-    if out_dev is None:
-        out_dev = torch.empty((T, shape.d), dtype=torch.bfloat16, device=dev)
+    assert x_host.dtype == torch.bfloat16 and not x_host.is_cuda and x_host.shape == (T, shape.d)
+    assert x_host.is_contiguous()
+    for w, rows, cols in ((w_gate, shape.I, shape.d), (w_up, shape.I, shape.d), (w_down, shape.d, shape.I)):
+        assert w.dtype == torch.bfloat16 and w.shape == (shape.E, rows, cols) and w.is_contiguous()
     if out_host is None:
         out_host = torch.empty((T, shape.d), dtype=torch.bfloat16, pin_memory=True)
-    with torch.cuda.stream(stream):
-        x_dev.copy_(x_host, non_blocking=True)
-        forward(x_dev, router_w, bias, w_gate, w_up, w_down, shape, out=out_dev, stream=stream)
-        out_host.copy_(out_dev, non_blocking=True)
-    stream.synchronize()
+    assert out_host.dtype == torch.bfloat16 and not out_host.is_cuda and out_host.shape == (T, shape.d)
+    abi.beam_moe_forward_host(shape, x_host, router_w, bias, w_gate, w_up, w_down, T, out_host, stream)
     return out_host
 
 

@@ -80,11 +80,22 @@ def hot_expert_ids(shape: MoEShape, n: int, seed: int = 0) -> torch.Tensor:
     return torch.randperm(shape.E, generator=g)[:n]
 
 
+# Experts drawn together per generator call: as many as fit this many FP32 bytes (all 256
+# Tiny experts in one draw; ten Beam experts).
+_DRAW_BYTES = 1 << 29
+
+
+def _expert_chunks(E: int, rows: int, fan_in: int):
+    n = max(1, min(E, _DRAW_BYTES // (rows * fan_in * 4)))
+    return [(e0, min(E, e0 + n)) for e0 in range(0, E, n)]
+
+
 def make_experts(shape: MoEShape, seed: int = 0, device="cpu"):
     """w_gate, w_up [E, I, d] and w_down [E, d, I], BF16, std 1/sqrt(fan_in).
 
-    Drawn one expert at a time in FP32, scaled, then rounded to BF16, so the peak extra
-    memory is one expert matrix in FP32.
+    Drawn in FP32 a few experts at a time (at most 512 MB of FP32 per draw), scaled, then
+    rounded to BF16: a handful of launches at the Tiny shape, bounded extra memory at
+    Beam's.
     """
     E, d, I = shape.E, shape.d, shape.I
     out = []
@@ -92,8 +103,9 @@ def make_experts(shape: MoEShape, seed: int = 0, device="cpu"):
         g = generator(seed, tag, device)
         w = torch.empty((E, rows, fan_in), device=device, dtype=torch.bfloat16)
         std = 1.0 / math.sqrt(fan_in)
-        for e in range(E):
-            w[e].copy_(torch.randn((rows, fan_in), generator=g, device=device, dtype=torch.float32).mul_(std))
+        for e0, e1 in _expert_chunks(E, rows, fan_in):
+            w[e0:e1].copy_(torch.randn((e1 - e0, rows, fan_in), generator=g, device=device,
+                                       dtype=torch.float32).mul_(std))
         out.append(w)
     return tuple(out)
 
@@ -114,7 +126,7 @@ def quantize_rows_fp8(w: torch.Tensor):
 def make_experts_fp8(shape: MoEShape, seed: int = 0, device="cpu"):
     """The experts of make_experts (same draws), quantised per row with quantize_rows_fp8:
     ((wg_q, wg_scale), (wu_q, wu_scale), (wd_q, wd_scale)) with q uint8 [E, rows, cols] and
-    scale float32 [E, rows]. Built one expert at a time (peak extra memory: one expert)."""
+    scale float32 [E, rows]. Drawn in the same chunks as make_experts."""
     E, d, I = shape.E, shape.d, shape.I
     out = []
     for tag, rows, fan_in in (("w_gate", I, d), ("w_up", I, d), ("w_down", d, I)):
@@ -122,9 +134,9 @@ def make_experts_fp8(shape: MoEShape, seed: int = 0, device="cpu"):
         q = torch.empty((E, rows, fan_in), device=device, dtype=torch.uint8)
         sc = torch.empty((E, rows), device=device, dtype=torch.float32)
         std = 1.0 / math.sqrt(fan_in)
-        for e in range(E):
-            w = torch.randn((rows, fan_in), generator=g, device=device, dtype=torch.float32).mul_(std)
-            q[e], sc[e] = quantize_rows_fp8(w.to(torch.bfloat16))
+        for e0, e1 in _expert_chunks(E, rows, fan_in):
+            w = torch.randn((e1 - e0, rows, fan_in), generator=g, device=device, dtype=torch.float32).mul_(std)
+            q[e0:e1], sc[e0:e1] = quantize_rows_fp8(w.to(torch.bfloat16))
         out.append((q, sc))
     return tuple(out)
 
