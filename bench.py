@@ -1,7 +1,7 @@
 """Benchmark of the Beam routed-MoE forward pass (libbeam_moe.so) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|tiny|T<n>]
-                    [--impl reference] [--no-secondary] [--weights bf16|fp8] [--sweep]
+                    [--impl reference] [--no-secondary] [--weights bf16|fp8] [--no-sweep]
 
 A step is one beam_moe_forward call over one batch of T tokens: router, dispatch,
 gate/up GEMM with SwiGLU, down GEMM, combine. Inputs and weights are synthetic, seeded,
@@ -13,9 +13,11 @@ time is the max over ranks.
 
 The default workload is Beam decode (T=16); one JSON line is printed by rank 0, carrying
 the dominant kernel's roofline, the CPU oracle's throughput on a bounded sample, the
-end-to-end number through host buffers, a secondary prefill (T=4096) measurement, and the
-same block on FP8 E4M3 expert weights (decode and prefill). --weights fp8 makes the FP8
-block the headline (used to profile it on smaller shapes).
+end-to-end number through host buffers (beam_moe_forward_host), and every other Beam
+workload, each with its own rooflines and clocks: prefill (T=4096), the skewed load
+(T=32768, 16 hot experts), the token-count sweep (T = 1 ... 16384) and the same block on
+FP8 E4M3 expert weights (decode and prefill). --weights fp8 makes the FP8 block the
+headline (used to profile it on smaller shapes).
 --impl reference times the CPU oracle itself as the reference arm.
 """
 from __future__ import annotations
@@ -218,12 +220,16 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
     roof["kernel_ms"] = stage_ms[dom]
     roof["traffic"] = TRAFFIC.get((name, fp8)) if shape.n_group == 8 else None
+    roof["frac_of_sustained"] = (kf / t_dom / 1e12 / pk["bf16_tflops_sustained"]) if not hbm_bound else None
 
     res = {
         "value": T * steps / (total_ms * 1e-3),
         "ms_per_step": ms_per_step,
         "roofline": roof,
         "ms_per_step_median": statistics.median(step_ms),
+        "ms_per_step_p10": float(np.percentile(step_ms, 10)),
+        "ms_per_step_p90": float(np.percentile(step_ms, 90)),
+        "near_tie_tokens": near_tie_count(shape, moe.router_logits(x, wr, shape).cpu().numpy(), b.cpu().numpy()),
         "layer_roofline": {"t_roof_ms": t_roof_s * 1e3, "frac": t_roof_s * 1e3 / ms_per_step,
                            "flops": layer_flops, "bytes": layer_bytes,
                            "tensor_frac_of_burst": layer_flops / (pk["bf16_tflops"] * 1e12) / (ms_per_step * 1e-3),
@@ -239,29 +245,52 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     return res
 
 
+def near_tie_count(shape, logits, bias, tie=1e-6):
+    """Tokens whose selection sits on a near-tie, from the library's own FP32 logits: a gap
+    below `tie` between neighbouring ranked group scores (the kept groups and the next one)
+    or between neighbouring ranked biased scores of the kept groups' experts (the picks and
+    the next one). On those tokens an ulp of the sigmoid can legitimately change a pick; the
+    parity tests accept any tie-consistent choice there. A diagnostic of the inputs only."""
+    T = logits.shape[0]
+    G, S, TG, K = shape.n_group, shape.E // shape.n_group, shape.topk_group, shape.top_k
+    s = (1.0 / (1.0 + np.exp(-logits.astype(np.float64)))).astype(np.float32)
+    c = (s + bias[None, :].astype(np.float32)).astype(np.float32)
+    top2 = -np.sort(-c.reshape(T, G, S), axis=2)[:, :, :2]
+    gs = (top2[:, :, 0] + top2[:, :, 1]).astype(np.float32)
+    order = np.argsort(-gs, axis=1, kind="stable")
+    gsr = np.take_along_axis(gs, order, axis=1).astype(np.float64)
+    ng = min(TG + 1, G)
+    g_gap = (gsr[:, :ng - 1] - gsr[:, 1:ng]).min(axis=1) if ng > 1 else np.full(T, np.inf)
+    kept = np.zeros((T, G), bool)
+    np.put_along_axis(kept, order[:, :TG], True, axis=1)
+    cc = np.where(np.repeat(kept, S, axis=1), c.astype(np.float64), -np.inf)
+    cs = -np.sort(-cc, axis=1)[:, :min(K + 1, TG * S)]
+    e_gap = np.where(np.isfinite(cs[:, 1:]), cs[:, :-1] - cs[:, 1:], np.inf).min(axis=1)
+    return int(((g_gap < tie) | (e_gap < tie)).sum())
+
+
 def measure_e2e(shape, T, x, wr, b, wg, wu, wd, steps, warmup, flush):
-    """Host tokens in, host output out, through the public call (moe.forward_host): the
-    H2D copy of the step's tokens, the forward pass and the D2H copy of its output are all
-    inside the timed region."""
+    """Host tokens in, host output out, through the library's host-buffer call
+    (beam_moe_forward_host via moe.forward_host): the H2D copy of the step's tokens, the
+    forward pass and the D2H copy of its output are all inside the timed region."""
     x_host = x.cpu().pin_memory()
     out_host = torch.empty((T, shape.d), dtype=torch.bfloat16, pin_memory=True)
     x_dev = torch.empty_like(x)
     out_dev = torch.empty((T, shape.d), dtype=torch.bfloat16, device=x.device)
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
-        moe.forward_host(x_host, wr, b, wg, wu, wd, shape, x_dev=x_dev, out_dev=out_dev, out_host=out_host,
-                         stream=stream)
+        moe.forward_host(x_host, wr, b, wg, wu, wd, shape, out_host=out_host, stream=stream)
     total = 0.0
     for _ in range(steps):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        moe.forward_host(x_host, wr, b, wg, wu, wd, shape, x_dev=x_dev, out_dev=out_dev, out_host=out_host,
-                         stream=stream)
+        moe.forward_host(x_host, wr, b, wg, wu, wd, shape, out_host=out_host, stream=stream)
         total += time.perf_counter() - t0
     total = max_over_ranks(total * 1e3) * 1e-3
     res = {"value": T * steps / total, "unit": "tokens/s", "h2d_bytes_per_step": T * shape.d * 2,
-           "d2h_bytes_per_step": T * shape.d * 2, "timer": "host wall clock around each synchronous step"}
+           "d2h_bytes_per_step": T * shape.d * 2, "call": "beam_moe_forward_host",
+           "timer": "host wall clock around each synchronous step"}
     # The same through moe.ForwardGraph: the call captured once, replayed per step.
     g = moe.ForwardGraph(x_dev, wr, b, wg, wu, wd, shape, out=out_dev)
     stream = torch.cuda.current_stream()
@@ -327,6 +356,15 @@ def max_over_ranks(v):
     return float(v)
 
 
+def summary(workload_name, r, steps):
+    """The per-workload object of the JSON line."""
+    keys = ("value", "ms_per_step", "ms_per_step_median", "ms_per_step_p10", "ms_per_step_p90", "roofline",
+            "layer_roofline", "stage_ms", "n_touched_experts", "near_tie_tokens", "gpu_launches", "clocks")
+    out = {"workload": workload_name, "unit": "tokens/s", "steps": steps}
+    out.update({k: r[k] for k in keys})
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -339,8 +377,8 @@ def main():
     ap.add_argument("--oracle-tokens", type=int, default=None)
     ap.add_argument("--n-group", type=int, default=8, help="expert groups of 32 (8 = Beam); fewer for profiling")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"], help="expert weights of the headline")
-    ap.add_argument("--sweep", action="store_true",
-                    help="also measure the token-count sweep T in {1, 8, 64, 256, 1024, 4096, 16384} (BF16)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the token-count sweep T in {1, 8, 64, 256, 1024, 4096, 16384} (BF16)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -391,10 +429,14 @@ def main():
         s_name, s_shape, s_T, s_hot = workload("prefill")
         s_steps = max(10, min(args.steps, 50))
         sec = measure(s_name, s_shape, s_T, s_hot, s_steps, args.warmup, experts, device, flush, pk, e2e=False)
-        secondary = {"workload": f"Beam prefill T={s_T}", "value": sec["value"], "unit": "tokens/s",
-                     "ms_per_step": sec["ms_per_step"], "steps": s_steps, "roofline": sec["roofline"],
-                     "layer_roofline": sec["layer_roofline"], "stage_ms": sec["stage_ms"],
-                     "n_touched_experts": sec["n_touched_experts"], "clocks": sec["clocks"]}
+        secondary = summary(f"Beam prefill T={s_T}", sec, s_steps)
+
+    skewed = None
+    if not args.no_secondary and name == "decode" and args.n_group == 8 and args.weights == "bf16":
+        k_name, k_shape, k_T, k_hot = workload("skewed")
+        k_steps = max(10, min(args.steps, 20))
+        r = measure(k_name, k_shape, k_T, k_hot, k_steps, args.warmup, experts, device, flush, pk, e2e=False)
+        skewed = summary(f"Beam skewed load T={k_T}, {k_hot} hot experts (+0.5 bias)", r, k_steps)
 
     fp8 = None
     if not args.no_secondary and name == "decode" and args.n_group == 8 and args.weights == "bf16":
@@ -406,26 +448,22 @@ def main():
             f_steps = args.steps if f_name == "decode" else max(10, min(args.steps, 50))
             r = measure(f_name, f_shape, f_T, f_hot, f_steps, args.warmup, experts, device, flush, pk, e2e=False,
                         experts_fp8=experts_fp8)
-            fp8[f_name] = {"workload": f"Beam {f_name} T={f_T}, FP8 E4M3 experts (per-row FP32 scales)",
-                           "value": r["value"], "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
-                           "steps": f_steps, "roofline": r["roofline"], "layer_roofline": r["layer_roofline"],
-                           "stage_ms": r["stage_ms"], "clocks": r["clocks"]}
+            fp8[f_name] = summary(f"Beam {f_name} T={f_T}, FP8 E4M3 experts (per-row FP32 scales)", r, f_steps)
         del experts_fp8
 
     sweep = None
-    if args.sweep and args.n_group == 8:
+    if not args.no_sweep and not args.no_secondary and args.n_group == 8 and args.weights == "bf16":
         sweep = []
-        for sT in (1, 8, 64, 256, 1024, 4096, 16384):
+        for sT in W.SWEEP_T:
             s_name, s_shape, _, _ = workload(f"T{sT}")
             s_steps = max(10, min(args.steps, 30))
             r = measure(s_name, s_shape, sT, 0, s_steps, args.warmup, experts, device, flush, pk, e2e=False)
             lr = r["layer_roofline"]
-            sweep.append({"T": sT, "value": r["value"], "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
-                          "layer_bound": "hbm" if lr["bytes"] / (pk["hbm_gbs"] * 1e9) >=
-                                         lr["flops"] / (pk["bf16_tflops"] * 1e12) else "tensor",
-                          "layer_roofline_frac": lr["frac"], "tensor_frac_of_burst": lr["tensor_frac_of_burst"],
-                          "expert_mlp": {k: r["roofline"][k] for k in ("bound", "achieved", "unit", "frac", "kernel_ms")},
-                          "n_touched_experts": r["n_touched_experts"], "clocks": r["clocks"]})
+            entry = summary(f"Beam T={sT}", r, s_steps)
+            entry["T"] = sT
+            entry["layer_bound"] = ("hbm" if lr["bytes"] / (pk["hbm_gbs"] * 1e9) >=
+                                    lr["flops"] / (pk["bf16_tflops"] * 1e12) else "tensor")
+            sweep.append(entry)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -439,6 +477,8 @@ def main():
             "metric": METRIC, "value": res["value"] * world, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
             "ms_per_step_median": res["ms_per_step_median"],
+            "ms_per_step_p10": res["ms_per_step_p10"], "ms_per_step_p90": res["ms_per_step_p90"],
+            "near_tie_tokens": res["near_tie_tokens"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) FP32 router, U(-0.1,0.1) bias, "
                     "BF16 experts std 1/sqrt(fan_in))",
@@ -462,6 +502,8 @@ def main():
         }
         if secondary:
             line["secondary"] = secondary
+        if skewed:
+            line["skewed"] = skewed
         if fp8:
             line["fp8_experts"] = fp8
         if sweep:

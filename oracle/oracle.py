@@ -209,13 +209,14 @@ class Oracle:
         return out
 
     def sublayer(self, shape, stream_bits, pre_gamma_bits, post_gamma_bits, eps, k, bias, experts, tokens,
-                 x_bits=None, logits=None, router_w=None, idx_in=None):
+                 x_bits=None, logits=None, router_w=None, idx_in=None, grouped=False):
         """The MoE sublayer for the rows `tokens` of a BF16 stream [T, d] (bit patterns),
         in the pages' order: x = RMSNorm_pre(stream) rounded to BF16 (the block's input
         hidden state), m = MoE(x), out = sqrt((k-1)/k) stream + RMSNorm_post(m) / sqrt(k).
         x_bits [T, d], if given, replaces the oracle's own rounded pre-norm output (so the
         rest can be checked given another implementation's BF16 input); logits / idx_in as
-        in forward(). Returns (out [n, d] FP64, x_rows [n, d] FP64 pre-norm before rounding)."""
+        in forward(). grouped: the MoE block through forward_grouped (for large token
+        samples). Returns (out [n, d] FP64, x_rows [n, d] FP64 pre-norm before rounding)."""
         stream_bits = _u16(stream_bits)
         tokens = np.ascontiguousarray(tokens, dtype=np.int64)
         T, d = stream_bits.shape
@@ -226,8 +227,12 @@ class Oracle:
         if x_bits is None:
             x_bits = np.zeros((T, d), np.uint16)
             x_bits[tokens] = self.round_bf16(x_rows)
-        m, _, _ = self.forward(shape, x_bits, bias, experts, tokens=tokens, router_w=router_w, logits=logits,
-                               idx_in=idx_in)
+        if grouped:
+            m, _ = self.forward_grouped(shape, x_bits, bias, experts, tokens, logits=logits, router_w=router_w,
+                                        idx_in=idx_in)
+        else:
+            m, _, _ = self.forward(shape, x_bits, bias, experts, tokens=tokens, router_w=router_w, logits=logits,
+                                   idx_in=idx_in)
         out = np.stack([self.residual(s64[i], self.rmsnorm(m[i], post_gamma_bits, eps), k)
                         for i in range(len(tokens))]) if len(tokens) else np.zeros((0, d))
         return out, x_rows

@@ -72,12 +72,24 @@ def check_routing(shape, gpu_logits, bias, gpu_idx, gpu_w):
     ok[flagged] = False
     np.testing.assert_array_equal(gpu_idx[ok], idx_o[ok], err_msg="expert indices differ on non-tie tokens")
     np.testing.assert_allclose(gpu_w[ok], w_o[ok], rtol=1e-6, atol=1e-7, err_msg="routing weights")
+    S = shape.E // shape.n_group
     for t in flagged:
         cg = dbg["c"][t, gpu_idx[t]].astype(np.float64)
         co = dbg["c"][t, idx_o[t]].astype(np.float64)
         assert len(set(gpu_idx[t].tolist())) == shape.top_k
         assert np.all(np.abs(np.sort(cg) - np.sort(co)) <= TIE), (t, gpu_idx[t], idx_o[t])
         assert np.all(cg[:-1] - cg[1:] >= -TIE), (t, "slot order")
+        # the picks lie in at most topk_group groups, each of which could be kept: its group
+        # score is within TIE of the oracle's topk_group-th best
+        groups = sorted(set((gpu_idx[t] // S).tolist()))
+        assert len(groups) <= shape.topk_group, (t, groups)
+        gs = dbg["gs"][t].astype(np.float64)
+        cut = np.sort(gs)[::-1][shape.topk_group - 1]
+        assert all(gs[g] >= cut - TIE for g in groups), (t, groups, gs)
+        # and every pick beats every candidate of those groups that was left out (to TIE)
+        cand = [e for g in groups for e in range(g * S, (g + 1) * S) if e not in set(gpu_idx[t].tolist())]
+        if cand:
+            assert dbg["c"][t, cand].astype(np.float64).max() <= cg.min() + TIE, (t, "a better candidate was left out")
     return flagged, dbg
 
 

@@ -343,6 +343,14 @@ def pin_forward_grouped_vs_per_token(O, seed=17):
     ref2, _, _ = O.forward(shape, xb, b.numpy(), experts, tokens=tokens, logits=logits, idx_in=sel)
     got2, _ = O.forward_grouped(shape, xb, b.numpy(), experts, tokens, logits=logits, idx_in=sel)
     assert np.abs(got2 - ref2).max() <= 1e-12 * max(np.abs(ref2).max(), 1.0)
+    # the sublayer with its MoE block evaluated the grouped way
+    g = torch.Generator().manual_seed(seed)
+    stream = torch.randn((48, shape.d), generator=g).mul_(3.0).to(torch.bfloat16)
+    gain = (1.0 + 0.1 * torch.randn(shape.d, generator=g)).to(torch.bfloat16)
+    args = (shape, _bits(stream), _bits(gain), _bits(gain), 1e-6, 5, b.numpy(), experts, tokens)
+    ref3, _ = O.sublayer(*args, router_w=wr.numpy())
+    got3, _ = O.sublayer(*args, router_w=wr.numpy(), grouped=True)
+    assert np.abs(got3 - ref3).max() <= 1e-12 * max(np.abs(ref3).max(), 1.0)
 
 
 def pin_e4m3_decoder_vs_torch(O):

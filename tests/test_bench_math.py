@@ -37,3 +37,22 @@ def test_single_process_helpers():
     assert (name, T, hot, shape.E) == ("prefill", 4096, 0, 256)
     name, shape, T, _ = bench.workload("decode", n_group=1)
     assert (name, shape.E, shape.topk_group, T) == ("decode_E32", 32, 1, 16)
+
+
+def test_near_tie_count_flags_only_near_ties():
+    """The bench's near-tie diagnostic: a token whose 8th and 9th biased scores differ by
+    less than 1e-6, or whose 4th and 5th group scores do, is counted; a token with clear
+    gaps is not."""
+    import numpy as np
+    s = W.BEAM
+    bias = np.zeros(s.E, np.float32)
+    clear = np.full(s.E, -6.0, np.float32)
+    clear[:8] = np.linspace(3.0, 1.0, 8)                 # eight clear picks in group 0
+    clear[32::32] = np.linspace(0.5, -1.0, 7)            # one clear leader in each other group
+    assert bench.near_tie_count(s, clear[None, :], bias) == 0
+    expert_tie = clear.copy()
+    expert_tie[8] = expert_tie[7]                         # 9th candidate equal to the 8th pick
+    assert bench.near_tie_count(s, expert_tie[None, :], bias) == 1
+    group_tie = clear.copy()
+    group_tie[4 * 32] = group_tie[3 * 32]                 # 5th group equal to the 4th kept one
+    assert bench.near_tie_count(s, np.stack([clear, group_tie, expert_tie]), bias) == 2

@@ -52,7 +52,7 @@ def _ep_worker(rank, world, port, results):
 
 def test_expert_parallel_shards_sum_to_the_block_over_gloo():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this (possibly CUDA) process
         results = m.dict()
         mp.spawn(_ep_worker, args=(2, port, results), nprocs=2, join=True)
         res = dict(results)

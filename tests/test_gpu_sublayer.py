@@ -81,12 +81,13 @@ def check_sublayer(layer, stream, pre, post, k, tokens, what):
     idx_r, _ = O.route(shape, logits[tokens], layer.b.cpu().numpy())
     needed |= set(np.unique(idx_r).tolist())
     experts = layer.experts(needed)
+    grouped = len(tokens) > 64
     ref, _ = O.sublayer(shape, O.bf16_bits(stream), O.bf16_bits(pre), O.bf16_bits(post), EPS, k,
-                        layer.b.cpu().numpy(), experts, tokens, x_bits=xb, logits=logits)
+                        layer.b.cpu().numpy(), experts, tokens, x_bits=xb, logits=logits, grouped=grouped)
     if len(flagged):
         ref2, _ = O.sublayer(shape, O.bf16_bits(stream), O.bf16_bits(pre), O.bf16_bits(post), EPS, k,
                              layer.b.cpu().numpy(), experts, tokens[flagged], x_bits=xb, logits=logits,
-                             idx_in=idx[tokens[flagged]])
+                             idx_in=idx[tokens[flagged]], grouped=grouped)
         ref[flagged] = ref2
     got = out.float().cpu().numpy()[tokens]
     frob = P.check_output(got, ref, what)
@@ -105,7 +106,7 @@ def test_tiny_sublayer_parity(T, k):
     check_sublayer(layer, stream, pre, post, k, np.arange(T), f"tiny sublayer T={T} k={k}")
 
 
-@pytest.mark.parametrize("T,k,n_check", [(16, 9, 16), (1024, 53, 16)])
+@pytest.mark.parametrize("T,k,n_check", [(16, 9, 16), (1024, 53, 256)])
 def test_beam_sublayer_parity(beam_experts, beam_host_cache, T, k, n_check):
     shape = W.BEAM
     x = W.make_tokens(shape, T, 0, "cuda")
