@@ -47,8 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # full-size workloads (seeded, so every run routes the same way), from one-pass ncu
 # captures of dram__bytes_read.sum and dram__bytes_write.sum; remove an entry when its
 # kernel changes after the capture. Keys: (workload name, FP8 experts).
-TRAFFIC = {("decode", False): 7000938240 + 4401408, ("prefill", False): 19823741440 + 495698688,
-           ("decode", True): 3504753408 + 3475200, ("prefill", True): 10755581952 + 492838656}
+TRAFFIC = {("decode", False): 7000938240 + 4401408, ("prefill", False): 19823741440 + 495698688}
 
 
 def peaks():

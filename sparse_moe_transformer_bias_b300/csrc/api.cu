@@ -105,7 +105,9 @@ int check_stream(cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------- stage timing
-enum Stage { kPreNorm, kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kExpert, kCombine, kNumStages };
+enum Stage {
+    kPreNorm, kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kExpert, kCombine, kFp8Prep, kNumStages
+};
 struct Timing {
     bool enabled = false;
     bool created = false;
@@ -175,6 +177,9 @@ struct Scratch {
     bf16* x_perm = nullptr;
     bf16* h = nullptr;
     bf16* y = nullptr;
+    float* xmax = nullptr;    // FP8 products: largest |x| per token
+    float* amax_h = nullptr;  // FP8 products: largest |h| per permuted row
+    uint8_t* x8 = nullptr;    // FP8 products: the two E4M3 pieces of every token row [T][2][d]
 };
 
 struct Carver {
@@ -191,7 +196,7 @@ struct Carver {
 
 // Lays scratch out from `base` (nullptr: size only). Returns the byte count.
 size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool forward, bool route_out,
-              bool pre_norm, char* base, Scratch* sc) {
+              bool pre_norm, bool fp8, char* base, Scratch* sc) {
     Carver c{base};
     const size_t pairs = static_cast<size_t>(T) * s.top_k;
     sc->x_norm = pre_norm ? c.take<bf16>(static_cast<size_t>(T) * s.d) : nullptr;
@@ -212,6 +217,11 @@ size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool
         sc->x_perm = c.take<bf16>(pairs * s.d);
         sc->h = c.take<bf16>(pairs * s.I);
         sc->y = c.take<bf16>(pairs * s.d);
+        if (fp8) {
+            sc->xmax = c.take<float>(static_cast<size_t>(T));
+            sc->amax_h = c.take<float>(pairs);
+            sc->x8 = c.take<uint8_t>(static_cast<size_t>(T) * 2 * s.d);
+        }
     }
     return c.off + 256;
 }
@@ -313,16 +323,16 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     Shape se = s;
     se.E = mode == 4 ? shard->e_end - shard->e_begin : s.E;
     const RouterPlan plan = router_plan(s, T, dev->num_sms);
-    const int bn_max = mode == 5 ? gemm_bn_max_fp8(s, T) : gemm_bn_max(s, T);
+    const int bn_max = mode == 5 ? gemm_bn_max_f8(s, T) : gemm_bn_max(s, T);
     const int max_tiles = dispatch_max_tiles(se, T, bn_max);
     const int rows = T * s.top_k;
     Scratch sc;
     const bool fwd = mode >= 2;
-    const size_t bytes = layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, nullptr, &sc);
+    const size_t bytes = layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, mode == 5, nullptr, &sc);
     void* mem = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, st);
     if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "scratch allocation of %zu bytes: %s", bytes, cudaGetErrorString(e));
-    layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, static_cast<char*>(mem), &sc);
+    layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, mode == 5, static_cast<char*>(mem), &sc);
     if ((e = maybe_poison(mem, bytes, st)) != cudaSuccess) {
         rc = fail(BEAM_MOE_ERR_CUDA, "scratch poison: %s", cudaGetErrorString(e));
         goto done;
@@ -340,9 +350,16 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
         LAUNCH(kSelect, launch_router_select(s, sc.partial, plan.splits, mode == 1 ? nullptr : bias, T, idx, w,
                                              mode == 1 ? logits : nullptr, st));
         if (fwd) {
+            // FP8 products: each token row is split into its two E4M3 pieces first; the
+            // dispatch then moves those rows (2d bytes each, as a BF16 row) instead of x.
+            const bf16* rows_src = x;
+            if (mode == 5) {
+                LAUNCH(kFp8Prep, launch_fp8_prep(x, s.d, T, sc.xmax, sc.x8, sc.amax_h, rows, dev->num_sms, st));
+                rows_src = reinterpret_cast<const bf16*>(sc.x8);
+            }
             if (T <= kSmallDispatchT) {
                 // one launch for the whole dispatch (timed as the count stage)
-                LAUNCH(kCount, launch_dispatch_small(s, e_lo, se.E, idx, T, bn_max, x, sc.expert_offset, sc.tiles,
+                LAUNCH(kCount, launch_dispatch_small(s, e_lo, se.E, idx, T, bn_max, rows_src, sc.expert_offset, sc.tiles,
                                                      sc.tile_done, sc.perm_src, sc.inv_slot, sc.x_perm, dev->status,
                                                      dev->num_sms, st));
             } else {
@@ -351,13 +368,15 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
                        launch_dispatch_scan(se.E, T, bn_max, sc.chunk, sc.expert_offset, sc.tiles, sc.tile_done, st));
                 LAUNCH(kScatter, launch_dispatch_scatter(s, e_lo, se.E, idx, T, sc.chunk, sc.perm_src, sc.inv_slot,
                                                          dev->status, st));
-                LAUNCH(kGather, launch_gather_rows(x, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
+                LAUNCH(kGather, launch_gather_rows(rows_src, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
                                                    dev->status, dev->num_sms, st));
             }
-            if (mode == 5)
-                LAUNCH(kExpert, launch_expert_mlp_fp8(se, *q8, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
-                                                      bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
-            else
+            if (mode == 5) {
+                LAUNCH(kExpert, launch_expert_mlp_f8(se, *q8, reinterpret_cast<const uint8_t*>(sc.x_perm), rows, T,
+                                                     sc.perm_src, sc.xmax, sc.amax_h,
+                                                     sc.tiles, sc.tile_done, max_tiles, bn_max, sc.h, sc.y,
+                                                     dev->status, dev->num_sms, st));
+            } else
                 LAUNCH(kExpert, launch_expert_mlp(se, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done,
                                                   max_tiles, bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
             if (mode == 4)

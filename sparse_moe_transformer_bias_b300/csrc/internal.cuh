@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "beam_moe.h"
@@ -135,6 +136,20 @@ int gemm_bn_max_fp8(const Shape& s, int T);
 cudaError_t launch_expert_mlp_fp8(const Shape& s, const Fp8Experts& q, const bf16* x_perm, int rows,
                                   const int4* tiles, int* tile_done, int max_tiles, int bn_max, bf16* h, bf16* y,
                                   int* status, int num_sms, cudaStream_t st);
+// FP8 E4M3 expert weights on the FP8 tensor cores (expert_mlp_fp8.cu): the same items and
+// outputs as launch_expert_mlp. Activations enter the products as two E4M3 pieces per row
+// under a power-of-two row scale: x8_perm holds the dispatched pieces of x (per permuted
+// row: p1 [d] then p2 [d], bytes), scaled by xmax[perm_src[row]]; h is split on chip with
+// amax_h[row] (raised by the gate/up epilogues; zero on entry). N-tiles of at most 128 rows.
+int gemm_bn_max_f8(const Shape& s, int T);
+cudaError_t launch_expert_mlp_f8(const Shape& s, const Fp8Experts& q, const uint8_t* x8_perm, int rows, int T,
+                                 const int* perm_src, const float* xmax, float* amax_h, const int4* tiles,
+                                 int* tile_done, int max_tiles, int bn_max, bf16* h, bf16* y, int* status,
+                                 int num_sms, cudaStream_t st);
+// For the T BF16 token rows of width d: xmax[t] = max_j |x[t][j]| and x8[t] = the row's two
+// E4M3 pieces (p1 [d] then p2 [d]) under the row's power-of-two scale; amax_h[0, rows) = 0.
+cudaError_t launch_fp8_prep(const bf16* x, int d, int T, float* xmax, uint8_t* x8, float* amax_h, int rows,
+                            int num_sms, cudaStream_t st);
 // Dense MLP (one "expert", every token in order): the work list and its capacity.
 int dense_max_tiles(int T, int bn_max);
 cudaError_t launch_dense_tiles(int T, int bn_max, int4* tiles, int* tile_done, cudaStream_t st);
@@ -190,6 +205,8 @@ struct BMaps {
 };
 // Encodes the maps for every box height up to bn_max (larger ones repeat m[0]).
 bool encode_bmaps(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int bn_max, const char** why);
+// As encode_bmaps for a byte matrix (E4M3 pieces): boxes of (16 << i) rows x 128 bytes.
+bool encode_bmaps_u8(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int box_max, const char** why);
 
 // Host helper: encode a 2-D BF16 tensor map (rows x cols, row-major) with the 128-byte
 // swizzle and a box of box_cols x box_rows. Returns false if the driver refuses it.

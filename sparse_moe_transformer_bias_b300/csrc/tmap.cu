@@ -106,4 +106,16 @@ bool encode_bmaps(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int 
     return true;
 }
 
+bool encode_bmaps_u8(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int box_max, const char** why) {
+    for (int i = 0; i < kBoxKinds; ++i) {
+        const uint32_t h = kBoxRows << i;
+        if (static_cast<int>(h) > box_max) {
+            b->m[i] = b->m[0];
+            continue;
+        }
+        if (!encode_tmap_u8_2d(&b->m[i], base, rows, cols, h, 128, why)) return false;
+    }
+    return true;
+}
+
 }  // namespace beam

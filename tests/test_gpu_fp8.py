@@ -1,7 +1,9 @@
 """FP8 expert weights: the CUDA block with E4M3 codes and per-row FP32 scales against the
 oracle on the same codes and scales (forward_fp8), element by element, on Tiny (every
-token, ragged counts, both N-tile sizes of the FP8 kernel) and on Beam shapes (sampled
-tokens at full size), plus a case that puts every finite E4M3 code through the widening."""
+token, ragged counts, every N-tile size of the FP8 kernel: 32 rows for T <= 32, 64 and
+128) and on Beam shapes (sampled tokens at full size), plus cases that put every finite
+E4M3 code through the FP8 tensor cores and that stretch the on-chip split of the BF16
+activations into two E4M3 pieces."""
 import numpy as np
 import pytest
 import torch
@@ -42,7 +44,7 @@ def tiny_fp8():
     return W.make_experts_fp8(W.TINY, seed=0, device="cuda")
 
 
-@pytest.mark.parametrize("T", [1, 16, 33, 129, 300, 1500])
+@pytest.mark.parametrize("T", [1, 16, 33, 129, 300, 1500, 2100])
 def test_tiny_fp8_parity(tiny_fp8, T):
     shape = W.TINY
     x = W.make_tokens(shape, T, 0, "cuda")
@@ -50,7 +52,7 @@ def test_tiny_fp8_parity(tiny_fp8, T):
     run_and_check(shape, x, wr, b, tiny_fp8, np.arange(T), f"tiny fp8 T={T}")
 
 
-def test_every_finite_code_is_widened_exactly():
+def test_every_finite_code_is_multiplied_exactly():
     """Gate, up and down codes cycle through all 254 finite E4M3 codes (zeros, subnormals,
     both signs, +-448) in every row, scales spread over several binades: the output must
     still match the oracle on every token."""
@@ -122,6 +124,50 @@ def test_fp8_close_to_bf16_block(tiny_fp8):
     got = moe.forward_fp8(x, wr, b, tiny_fp8, shape).double()
     rel = float((got - ref).norm() / ref.norm())
     assert rel < 0.1, rel
+
+
+def test_activation_rows_with_a_wide_range():
+    """The on-chip split of each BF16 token row into two E4M3 pieces under one power-of-two
+    row scale: rows whose largest entry is 2^12 times their typical entry (their small
+    entries then fall into the E4M3 subnormal range of the pieces), rows of one tiny
+    magnitude (2^-40), a row with a single nonzero entry and an all-zero row. The experts
+    have power-of-two row scales, so their dequantised weights are exact BF16 values and
+    the BF16 block on those weights computes the same products: the FP8 block must agree
+    with it to within two BF16 steps of each row's largest output, and both must match the
+    oracle to the output tolerance's Frobenius bound row by row. (With such outliers the
+    BF16 rounding of h and y, which both blocks share, exceeds the per-element bound on
+    elements that cancel, so that bound is checked on the ordinary rows only.)"""
+    import pins
+    from oracle import oracle as O
+    shape = W.TINY
+    fp8, bf = pins._pow2_fp8_experts(shape, 3)
+    q8 = tuple((q.cuda(), s.cuda()) for q, s in fp8)
+    wg, wu, wd = (w.cuda() for w in bf)
+    T = 40
+    x = W.make_tokens(shape, T, 8, "cuda").float()
+    x[0:8, 3] = 4096.0
+    x[8:16, 100:110] = -3000.0
+    x[16:24] *= 2.0 ** -40
+    x[24] = 0.0
+    x[24, 7] = 1.5
+    x[25] = 0.0
+    x = x.to(torch.bfloat16)
+    wr, b = W.make_router(shape, 8, "cuda")
+    o8 = moe.forward_fp8(x, wr, b, q8, shape).double().cpu().numpy()
+    o16 = moe.forward(x, wr, b, wg, wu, wd, shape).double().cpu().numpy()
+    logits = moe.router_logits(x, wr, shape).cpu().numpy()
+    abi.beam_moe_device_status()
+    experts = lambda e: (O.bf16_bits(bf[0][e]), O.bf16_bits(bf[1][e]), O.bf16_bits(bf[2][e]))  # noqa: E731
+    ref, _, _ = O.forward(shape, O.bf16_bits(x), b.cpu().numpy(), experts, logits=logits)
+    assert np.all(o8[25] == 0.0) and np.all(o16[25] == 0.0)
+    for t in range(T):
+        if t == 25:
+            continue
+        top = np.abs(o16[t]).max()
+        assert np.abs(o8[t] - o16[t]).max() <= 2.0 ** -7 * top, t
+        for o in (o8, o16):
+            assert np.linalg.norm(o[t] - ref[t]) <= P.FROB * np.linalg.norm(ref[t]), t
+    P.check_output(o8[16:], ref[16:], "wide-range activations, ordinary rows")
 
 
 @pytest.fixture(scope="module")

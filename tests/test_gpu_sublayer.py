@@ -145,7 +145,7 @@ def test_sublayer_in_place_and_deterministic():
     moe.sublayer_forward(s2, pre, post, EPS, k, wr, b, wg, wu, wd, shape, out=s2)
     torch.cuda.synchronize()
     assert torch.equal(a, c) and torch.equal(a, s2)
-    assert abi.beam_moe_last_launch_count() == len(abi.STAGES)
+    assert abi.beam_moe_last_launch_count() == len(abi.STAGES) - 1  # every stage but the FP8 prep
 
 
 def test_sublayer_keeps_the_stream_scale():
