@@ -400,3 +400,73 @@ int oracle_expert_fp8(int d, int I, const double *x, const uint8_t *wg_q, const 
     free(h);
     return ORACLE_OK;
 }
+
+/*
+ * NVFP4 (the NVFP4 checkpoint: [Glonce] Hardware paragraph, about 280 GB on Blackwell;
+ * [Atech] "about 4.5 bits with scales"). The pages give the format's name only; this
+ * reading takes the public NVFP4 layout: 4-bit E2M1 codes in blocks of 16 consecutive
+ * elements along a row, one E4M3 scale per block, and one FP32 scale per tensor (here: per
+ * expert matrix). 4 + 8/16 = 4.5 bits per weight.
+ * E2M1 from the format's definition: bit 3 sign, bits 2-1 exponent with bias 1, bit 0
+ * mantissa; exponent 0 is subnormal (m * 0.5).
+ */
+static double e2m1_value(uint8_t c)
+{
+    const int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    const double v = e == 0 ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Values of n E2M1 codes given one per byte (low 4 bits). */
+int oracle_e2m1_decode(int64_t n, const uint8_t *c, double *out)
+{
+    if (n < 0 || (n && (!c || !out))) return ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < n; i++) out[i] = e2m1_value(c[i] & 15);
+    return ORACLE_OK;
+}
+
+/*
+ * Element c of an NVFP4 matrix row: codes are packed two per byte, element 2k in the low
+ * half of byte k and element 2k+1 in its high half (the reading of the packing); the block
+ * scale of element c is the E4M3 code bs[c / 16]:
+ *   W[r][c] = t * e4m3(bs[r][c / 16]) * e2m1(code of element c of row r)
+ */
+static double nvfp4_value(const uint8_t *q_row, const uint8_t *bs_row, double t, int c)
+{
+    const uint8_t byte = q_row[c / 2];
+    const uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
+    return t * e4m3_value(bs_row[c / 16]) * e2m1_value(code);
+}
+
+/*
+ * One SwiGLU expert with NVFP4 weights (same form as oracle_expert, all in FP64):
+ *   wg_q, wu_q [I][d/2] packed codes with block scales gs, us [I][d/16] and tensor scales
+ *   gt, ut; wd_q [d][I/2] with ds [d][I/16] and dt. d and I multiples of 16.
+ */
+int oracle_expert_nvfp4(int d, int I, const double *x, const uint8_t *wg_q, const uint8_t *gs, double gt,
+                        const uint8_t *wu_q, const uint8_t *us, double ut, const uint8_t *wd_q, const uint8_t *ds,
+                        double dt, double *y)
+{
+    if (d <= 0 || I <= 0 || d % 16 || I % 16 || !x || !wg_q || !gs || !wu_q || !us || !wd_q || !ds || !y)
+        return ORACLE_BAD_ARG;
+    double *h = (double *)malloc(sizeof(double) * I);
+    if (!h) return ORACLE_NO_MEM;
+    for (int i = 0; i < I; i++) {
+        double g = 0.0, u = 0.0;
+        const uint8_t *gq = wg_q + (int64_t)i * (d / 2), *gb = gs + (int64_t)i * (d / 16);
+        const uint8_t *uq = wu_q + (int64_t)i * (d / 2), *ub = us + (int64_t)i * (d / 16);
+        for (int j = 0; j < d; j++) {
+            g += x[j] * nvfp4_value(gq, gb, gt, j);
+            u += x[j] * nvfp4_value(uq, ub, ut, j);
+        }
+        h[i] = g * u / (1.0 + exp(-g));
+    }
+    for (int j = 0; j < d; j++) {
+        double acc = 0.0;
+        const uint8_t *dq = wd_q + (int64_t)j * (I / 2), *db = ds + (int64_t)j * (I / 16);
+        for (int i = 0; i < I; i++) acc += h[i] * nvfp4_value(dq, db, dt, i);
+        y[j] = acc;
+    }
+    free(h);
+    return ORACLE_OK;
+}

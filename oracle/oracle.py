@@ -96,10 +96,13 @@ class Oracle:
         L.oracle_e4m3_decode.argtypes = [i64, P, P]
         L.oracle_expert_fp8.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P]
         L.oracle_residual.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P]
+        dbl = ctypes.c_double
+        L.oracle_e2m1_decode.argtypes = [i64, P, P]
+        L.oracle_expert_nvfp4.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, dbl, P, P, dbl, P, P, dbl, P]
         L.oracle_round_bf16.argtypes = [i64, P, P]
         for f in (L.oracle_check_cfg, L.oracle_router_logits, L.oracle_route, L.oracle_expert, L.oracle_forward,
                   L.oracle_rmsnorm, L.oracle_residual, L.oracle_round_bf16, L.oracle_e4m3_decode,
-                  L.oracle_expert_fp8):
+                  L.oracle_expert_fp8, L.oracle_e2m1_decode, L.oracle_expert_nvfp4):
             f.restype = ctypes.c_int
         self.L = L
         self.path = path
@@ -255,11 +258,31 @@ class Oracle:
                                         _ptr(scs[1]), _ptr(arrs[2]), _ptr(scs[2]), _ptr(y)), "expert_fp8")
         return y
 
-    def forward_fp8(self, shape, x_bits, bias, experts_q, tokens, logits=None, router_w=None, idx_in=None):
-        """The MoE block with FP8 experts for the rows `tokens`: the same routing as
-        forward() (from `logits` if given), experts evaluated by expert_fp8, weighted sum in
-        FP64 in slot order. experts_q: e -> (wg_q, gs, wu_q, us, wd_q, ds). idx_in replaces
-        the selection for the given rows (weights from the oracle's own sigmoid scores)."""
+    def e2m1_decode(self, codes) -> np.ndarray:
+        """FP64 values of E2M1 (FP4) codes, one per byte (low 4 bits), any shape."""
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, np.float64)
+        _check(self.L.oracle_e2m1_decode(c.size, _ptr(c), _ptr(out)), "e2m1_decode")
+        return out
+
+    def expert_nvfp4(self, shape, x_row, gate, up, down) -> np.ndarray:
+        """One SwiGLU expert with NVFP4 weights on one FP64 row. gate, up, down are (codes,
+        block scales, tensor scale): codes uint8 [rows, cols/2] (two per byte, element 2k in
+        the low half), block scales E4M3 codes uint8 [rows, cols/16], tensor scale a float."""
+        x_row = np.ascontiguousarray(x_row, dtype=np.float64)
+        keep = [np.ascontiguousarray(a, dtype=np.uint8) for g in (gate, up, down) for a in g[:2]]
+        ptrs = [_ptr(k) for k in keep]
+        y = np.empty(shape.d, np.float64)
+        _check(self.L.oracle_expert_nvfp4(shape.d, shape.I, _ptr(x_row), ptrs[0], ptrs[1], float(gate[2]), ptrs[2],
+                                          ptrs[3], float(up[2]), ptrs[4], ptrs[5], float(down[2]), _ptr(y)),
+               "expert_nvfp4")
+        return y
+
+    def _forward_with(self, shape, x_bits, bias, expert_of, tokens, logits=None, router_w=None, idx_in=None):
+        """The MoE block for the rows `tokens` with the expert evaluated by expert_of(x_row, e)
+        (an FP64 row in, an FP64 row out): the same routing as forward() (from `logits` if
+        given), weights from the oracle's own sigmoid scores, weighted sum in FP64 in slot
+        order. idx_in replaces the selection for the given rows."""
         x_bits = _u16(x_bits)
         tokens = np.ascontiguousarray(tokens, dtype=np.int64)
         lg = _f32(logits)[tokens] if logits is not None else self.router_logits(shape, x_bits[tokens], router_w)
@@ -274,8 +297,21 @@ class Oracle:
         for n, t in enumerate(tokens):
             xr = (x_bits[t].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
             for k in range(shape.top_k):
-                out[n] += w64[n, k] * self.expert_fp8(shape, xr, *experts_q(int(idx[n, k])))
+                out[n] += w64[n, k] * expert_of(xr, int(idx[n, k]))
         return out, idx
+
+    def forward_fp8(self, shape, x_bits, bias, experts_q, tokens, logits=None, router_w=None, idx_in=None):
+        """The MoE block with FP8 experts for the rows `tokens` (composition of _forward_with),
+        experts evaluated by expert_fp8. experts_q: e -> (wg_q, gs, wu_q, us, wd_q, ds)."""
+        return self._forward_with(shape, x_bits, bias, lambda xr, e: self.expert_fp8(shape, xr, *experts_q(e)),
+                                  tokens, logits=logits, router_w=router_w, idx_in=idx_in)
+
+    def forward_nvfp4(self, shape, x_bits, bias, experts_q, tokens, logits=None, router_w=None, idx_in=None):
+        """The MoE block with NVFP4 experts for the rows `tokens` (composition of
+        _forward_with), experts evaluated by expert_nvfp4. experts_q: e -> (gate, up, down),
+        each (codes, block scales, tensor scale) as expert_nvfp4 takes them."""
+        return self._forward_with(shape, x_bits, bias, lambda xr, e: self.expert_nvfp4(shape, xr, *experts_q(e)),
+                                  tokens, logits=logits, router_w=router_w, idx_in=idx_in)
 
     def forward_grouped(self, shape, x_bits, bias, experts, tokens, logits=None, router_w=None, idx_in=None):
         """forward() for many tokens at Beam size: the same routing (this oracle's, from
@@ -389,6 +425,18 @@ def forward_grouped(*a, **k):
 
 def forward_fp8(*a, **k):
     return default().forward_fp8(*a, **k)
+
+
+def e2m1_decode(*a, **k):
+    return default().e2m1_decode(*a, **k)
+
+
+def expert_nvfp4(*a, **k):
+    return default().expert_nvfp4(*a, **k)
+
+
+def forward_nvfp4(*a, **k):
+    return default().forward_nvfp4(*a, **k)
 
 
 def bf16_bits(t) -> np.ndarray:

@@ -141,6 +141,51 @@ def make_experts_fp8(shape: MoEShape, seed: int = 0, device="cpu"):
     return tuple(out)
 
 
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)  # FP4 E2M1 codes 0..7
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """NVFP4 checkpoint recipe for weight matrices w [..., rows, cols] (cols a multiple of
+    16); the pages name the format but give no recipe, this is the plainest public one:
+    one FP32 tensor scale per matrix t = max|w| / (448 * 6); per block of 16 consecutive
+    elements of a row, an E4M3 scale bs = (block max|w|) / 6 / t rounded to E4M3 by torch;
+    codes = the E2M1 magnitude nearest to |w| / (t * bs) (ties to the smaller), bit 3 the
+    sign, packed two per byte (element 2k in the low half of byte k). Returns (codes uint8
+    [..., rows, cols/2], block scales as E4M3 codes uint8 [..., rows, cols/16], t float32
+    [...])."""
+    wf = w.float()
+    *lead, rows, cols = wf.shape
+    t = (wf.abs().amax(dim=(-2, -1)) / (448.0 * 6.0)).clamp_min(1e-30)
+    blocks = wf.reshape(*lead, rows, cols // 16, 16)
+    bs = (blocks.abs().amax(dim=-1) / 6.0 / t[..., None, None]).to(torch.float8_e4m3fn)
+    denom = (t[..., None, None] * bs.float()).unsqueeze(-1)
+    v = torch.where(denom > 0, blocks / torch.where(denom > 0, denom, torch.ones_like(denom)), torch.zeros_like(blocks))
+    mids = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], device=w.device)
+    mag = torch.bucketize(v.abs().contiguous(), mids)                      # 0..7
+    code = (mag | ((v < 0) & (mag > 0)).to(mag.dtype) << 3).to(torch.uint8).reshape(*lead, rows, cols)
+    packed = code[..., 0::2] | (code[..., 1::2] << 4)
+    return packed.contiguous(), bs.view(torch.uint8).contiguous(), t.float()
+
+
+def make_experts_nvfp4(shape: MoEShape, seed: int = 0, device="cpu"):
+    """The experts of make_experts (same draws), quantised with quantize_nvfp4, one tensor
+    scale per expert matrix: ((wg_q, wg_bs, wg_t), (wu_q, wu_bs, wu_t), (wd_q, wd_bs, wd_t))
+    with codes uint8 [E, rows, cols/2], block scales uint8 [E, rows, cols/16], t float32 [E]."""
+    E, d, I = shape.E, shape.d, shape.I
+    out = []
+    for tag, rows, fan_in in (("w_gate", I, d), ("w_up", I, d), ("w_down", d, I)):
+        g = generator(seed, tag, device)
+        q = torch.empty((E, rows, fan_in // 2), device=device, dtype=torch.uint8)
+        bs = torch.empty((E, rows, fan_in // 16), device=device, dtype=torch.uint8)
+        t = torch.empty((E,), device=device, dtype=torch.float32)
+        std = 1.0 / math.sqrt(fan_in)
+        for e0, e1 in _expert_chunks(E, rows, fan_in):
+            w = torch.randn((e1 - e0, rows, fan_in), generator=g, device=device, dtype=torch.float32).mul_(std)
+            q[e0:e1], bs[e0:e1], t[e0:e1] = quantize_nvfp4(w.to(torch.bfloat16))
+        out.append((q, bs, t))
+    return tuple(out)
+
+
 def sample_tokens(T: int, n: int, seed: int = 0) -> torch.Tensor:
     """A seeded, sorted subset of n distinct token indices out of T (all of them if n >= T)."""
     if n >= T:

@@ -31,6 +31,7 @@ import torch
 from sparse_moe_transformer_bias_b300 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "routing_handworked.json")
+E2M1_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "e2m1_values.json")
 
 
 def small_shape(**kw):
@@ -453,6 +454,100 @@ def pin_forward_fp8_identical_experts(orc, seed=19):
     want = shape.scale * ((torch.nn.functional.silu(x64 @ wg64.T) * (x64 @ wu64.T)) @ wd64.T)
     np.testing.assert_allclose(out, want.numpy(), rtol=1e-10, atol=1e-12)
 
+
+def _e2m1_table():
+    return torch.tensor(json.load(open(E2M1_GOLDEN))["values"], dtype=torch.float64)
+
+
+def nvfp4_dequant_torch(q, bs, t):
+    """NVFP4 weights [rows, cols] in float64 from codes [rows, cols/2] (element 2k in the low
+    half of byte k), E4M3 block scales [rows, cols/16] and a tensor scale, with the golden
+    E2M1 table and torch's float8_e4m3fn (no oracle code)."""
+    q = torch.as_tensor(q)
+    rows, half = q.shape
+    codes = torch.stack([q & 15, q >> 4], dim=-1).reshape(rows, 2 * half).long()
+    vals = _e2m1_table()[codes].reshape(rows, -1, 16)
+    scales = torch.as_tensor(bs).view(torch.float8_e4m3fn).to(torch.float64).unsqueeze(-1)
+    return (vals * scales).reshape(rows, 2 * half) * float(t)
+
+
+def pin_e2m1_decoder_table(O):
+    """Every E2M1 code decodes to the value the format's table gives (signed zero included)."""
+    spec = json.load(open(E2M1_GOLDEN))
+    got = O.e2m1_decode(np.asarray(spec["codes"], np.uint8))
+    want = np.asarray(spec["values"], np.float64)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(np.signbit(got), np.signbit(want))
+
+
+def pin_nvfp4_expert_vs_torch(O, seed=20):
+    """The NVFP4 expert equals the SwiGLU of torch float64 on the weights dequantised here
+    (golden E2M1 table, torch E4M3 block scales, tensor scale), for a quantised Tiny expert;
+    and the quantisation stays near the BF16 expert it came from (a sanity bound)."""
+    shape = W.TINY
+    mats = W.make_experts_nvfp4(shape, seed)
+    e = 11
+    parts = [(m[0][e].numpy(), m[1][e].numpy(), float(m[2][e])) for m in mats]
+    wg64, wu64, wd64 = (nvfp4_dequant_torch(*p) for p in parts)
+    x = torch.randn(shape.d, generator=torch.Generator().manual_seed(seed), dtype=torch.float64)
+    got = O.expert_nvfp4(shape, x.numpy(), *parts)
+    want = (torch.nn.functional.silu(wg64 @ x) * (wu64 @ x)) @ wd64.T
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-10, atol=1e-12)
+    wg, wu, wd = (w[e].double() for w in W.make_experts(shape, seed))
+    ref = (torch.nn.functional.silu(wg @ x) * (wu @ x)) @ wd.T
+    assert float((want - ref).norm() / ref.norm()) < 0.25
+
+
+def _exact_nvfp4_experts(shape, seed):
+    """NVFP4 experts whose dequantised weights are exact BF16 values: random codes over all
+    16 E2M1 values, block scales among the E4M3 codes with exponent field 5..9 (2^-2 .. 2^2
+    times 1..1.875), tensor scales powers of two. A product of an E2M1 value (2 significant
+    bits), an E4M3 value (4) and a power of two has at most 6, so it is a BF16 number.
+    Returns the NVFP4 parts per matrix and the equal BF16 experts."""
+    g = torch.Generator().manual_seed(seed)
+    parts, bf = [], []
+    for rows, cols in ((shape.I, shape.d), (shape.I, shape.d), (shape.d, shape.I)):
+        q = torch.randint(0, 256, (shape.E, rows, cols // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+        bs = ((torch.randint(5, 10, (shape.E, rows, cols // 16), generator=g) << 3) |
+              torch.randint(0, 8, (shape.E, rows, cols // 16), generator=g)).to(torch.uint8)
+        t = torch.exp2(torch.randint(-5, -2, (shape.E,), generator=g).float()) / math.sqrt(cols)
+        t = torch.exp2(torch.round(torch.log2(t)))
+        deq = torch.stack([nvfp4_dequant_torch(q[e], bs[e], t[e]) for e in range(shape.E)])
+        wb = deq.to(torch.bfloat16)
+        assert torch.equal(wb.double(), deq), "such an NVFP4 weight must be a BF16 value"
+        parts.append((q, bs, t))
+        bf.append(wb)
+    return tuple(parts), tuple(bf)
+
+
+def pin_forward_nvfp4_equals_bf16_block(orc, seed=21):
+    """The NVFP4 block's composition against the BF16 block: on NVFP4 experts whose
+    dequantised weights are exact BF16 values, forward_nvfp4 must equal forward on those
+    BF16 weights, with the oracle's own routing and with a selection handed in."""
+    shape = W.MoEShape(d=64, I=48)
+    T = 5
+    x = W.make_tokens(shape, T, seed)
+    wr, b = W.make_router(shape, seed)
+    parts, (wg, wu, wd) = _exact_nvfp4_experts(shape, seed)
+    xb = _bits(x)
+    experts_q = lambda e: tuple((p[0][e].numpy(), p[1][e].numpy(), float(p[2][e])) for p in parts)  # noqa: E731
+    experts_b = lambda e: (_bits(wg[e]), _bits(wu[e]), _bits(wd[e]))  # noqa: E731
+    tokens = np.arange(T)
+    logits = orc.router_logits(shape, xb, wr.numpy())
+    ref, idx_r, _ = orc.forward(shape, xb, b.numpy(), experts_b, tokens=tokens, logits=logits)
+    got, idx_g = orc.forward_nvfp4(shape, xb, b.numpy(), experts_q, tokens, logits=logits)
+    np.testing.assert_array_equal(idx_g, idx_r)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    sel = np.roll(idx_r, 2, axis=1).copy()
+    sel[:, 1] = (sel[:, 1] + 77) % shape.E
+    for t in range(T):
+        assert len(set(sel[t].tolist())) == shape.top_k
+    ref2, _, _ = orc.forward(shape, xb, b.numpy(), experts_b, tokens=tokens, logits=logits, idx_in=sel)
+    got2, idx2 = orc.forward_nvfp4(shape, xb, b.numpy(), experts_q, tokens, logits=logits, idx_in=sel)
+    np.testing.assert_array_equal(idx2, sel)
+    np.testing.assert_allclose(got2, ref2, rtol=1e-12, atol=1e-12 * np.abs(ref2).max())
+
+
 ALL_CHECKS = [
     check_golden_cases, check_invariants, check_sigmoid_and_bias, check_group_scores_vs_topk,
     check_group_choice_brute_force, check_selection_brute_force_small, check_plain_topk_reduction,
@@ -461,4 +556,5 @@ ALL_CHECKS = [
     pin_rmsnorm_library, pin_rmsnorm_closed_forms, pin_residual_is_scaled_sum, pin_round_bf16_vs_torch,
     pin_sublayer_composition, pin_e4m3_decoder_vs_torch, pin_fp8_expert_vs_torch, pin_forward_grouped_vs_per_token,
     pin_forward_fp8_equals_bf16_block, pin_forward_fp8_identical_experts,
+    pin_e2m1_decoder_table, pin_nvfp4_expert_vs_torch, pin_forward_nvfp4_equals_bf16_block,
 ]

@@ -46,6 +46,11 @@ MUTANTS = [
     ("fp8_down_scale_dropped", "acc += h[i] * ((double)ds[j] * e4m3_value(wd_q[(int64_t)j * I + i]));",
      "acc += h[i] * e4m3_value(wd_q[(int64_t)j * I + i]);"),
     ("fp8_silu_on_up", "h[i] = g * u / (1.0 + exp(-g));", "h[i] = g * u / (1.0 + exp(-u));"),
+    ("e2m1_exponent_bias_off", "ldexp(1.0 + 0.5 * (double)m, e - 1)", "ldexp(1.0 + 0.5 * (double)m, e - 2)"),
+    ("e2m1_subnormal_not_halved", "e == 0 ? 0.5 * (double)m :", "e == 0 ? (double)m :"),
+    ("nvfp4_nibbles_swapped", "(c & 1) ? (byte >> 4) : (byte & 15)", "(c & 1) ? (byte & 15) : (byte >> 4)"),
+    ("nvfp4_blocks_of_32", "e4m3_value(bs_row[c / 16])", "e4m3_value(bs_row[c / 32])"),
+    ("nvfp4_tensor_scale_dropped", "return t * e4m3_value(bs_row[c / 16])", "return e4m3_value(bs_row[c / 16])"),
     ("fp8_up_scale_from_gate", "u += x[j] * ((double)us[i] * e4m3_value(wu_q[(int64_t)i * d + j]));",
      "u += x[j] * ((double)gs[i] * e4m3_value(wu_q[(int64_t)i * d + j]));"),
 ]
@@ -67,14 +72,15 @@ def test_mutant_is_caught(name, old, new):
 
 
 # Mistakes in the Python compositions of the oracle: (name, method, text, replacement).
+# _forward_with is the block composition of the FP8 and NVFP4 experts.
 PY_MUTANTS = [
-    ("fp8_weights_from_biased_score", "forward_fp8", 's = dbg["s"].astype(np.float64)',
+    ("quant_weights_from_biased_score", "_forward_with", 's = dbg["s"].astype(np.float64)',
      's = dbg["c"].astype(np.float64)'),
-    ("fp8_given_weights_scale_missing", "forward_fp8", "w64 = shape.scale * picked / picked.sum(axis=1, keepdims=True)",
+    ("quant_given_weights_scale_missing", "_forward_with", "w64 = shape.scale * picked / picked.sum(axis=1, keepdims=True)",
      "w64 = picked / picked.sum(axis=1, keepdims=True)"),
-    ("fp8_combine_drops_slot", "forward_fp8", "for k in range(shape.top_k):",
+    ("quant_combine_drops_slot", "_forward_with", "for k in range(shape.top_k):",
      "for k in range(shape.top_k - 1):"),
-    ("fp8_weights_not_normalised", "forward_fp8", "w64 = dbg[\"w64\"]", "w64 = dbg[\"w64\"] * 1.001"),
+    ("quant_weights_not_normalised", "_forward_with", "w64 = dbg[\"w64\"]", "w64 = dbg[\"w64\"] * 1.001"),
 ]
 
 
