@@ -45,7 +45,10 @@ MUTANTS = [
     ("e4m3_subnormal_scale", "if (e == 0) v = ldexp((double)m / 8.0, -6);", "if (e == 0) v = ldexp((double)m / 8.0, -7);"),
     ("fp8_down_scale_dropped", "acc += h[i] * ((double)ds[j] * e4m3_value(wd_q[(int64_t)j * I + i]));",
      "acc += h[i] * e4m3_value(wd_q[(int64_t)j * I + i]);"),
-    ("fp8_silu_on_up", "h[i] = g * u / (1.0 + exp(-g));", "h[i] = g * u / (1.0 + exp(-u));"),
+    ("fp8_silu_on_up", "e4m3_value(wu_q[(int64_t)i * d + j]));\n        }\n        h[i] = g * u / (1.0 + exp(-g));",
+     "e4m3_value(wu_q[(int64_t)i * d + j]));\n        }\n        h[i] = g * u / (1.0 + exp(-u));"),
+    ("nvfp4_silu_on_up", "nvfp4_value(uq, ub, ut, j);\n        }\n        h[i] = g * u / (1.0 + exp(-g));",
+     "nvfp4_value(uq, ub, ut, j);\n        }\n        h[i] = g * u / (1.0 + exp(-u));"),
     ("e2m1_exponent_bias_off", "ldexp(1.0 + 0.5 * (double)m, e - 1)", "ldexp(1.0 + 0.5 * (double)m, e - 2)"),
     ("e2m1_subnormal_not_halved", "e == 0 ? 0.5 * (double)m :", "e == 0 ? (double)m :"),
     ("nvfp4_nibbles_swapped", "(c & 1) ? (byte >> 4) : (byte & 15)", "(c & 1) ? (byte & 15) : (byte >> 4)"),
