@@ -136,12 +136,18 @@ def make_layer(shape, T, hot, device, experts=None, seed=0):
     return x, wr, b, experts
 
 
-def algorithmic(shape, T, n_touched, rows, fp8=False):
+def algorithmic(shape, T, n_touched, rows, fp8=False, fp4=False):
     """Algorithmic FLOPs and bytes of the whole layer and of the expert kernel (one launch:
     gate/up + SwiGLU and down over the touched experts' weights). FP8 experts: one byte
-    per weight plus one FP32 scale per weight row."""
+    per weight plus one FP32 scale per weight row. NVFP4 experts: half a byte per weight,
+    one byte of block scale per 16 weights and one FP32 tensor scale per matrix."""
     d, I, E, K = shape.d, shape.I, shape.E, shape.top_k
-    w_bytes = n_touched * (3 * d * I + (2 * I + d) * 4) if fp8 else n_touched * 3 * d * I * 2
+    if fp4:
+        w_bytes = n_touched * (3 * d * I // 2 + 3 * d * I // 16 + 3 * 4)
+    elif fp8:
+        w_bytes = n_touched * (3 * d * I + (2 * I + d) * 4)
+    else:
+        w_bytes = n_touched * 3 * d * I * 2
     layer_flops = T * (K * 3 * 2 * d * I + 2 * d * E)
     layer_bytes = w_bytes + E * d * 4 + E * 4 + 2 * T * d * 2 + T * K * 8
     # weights once; x_perm read, h written and read back, y (BF16) written
@@ -150,8 +156,10 @@ def algorithmic(shape, T, n_touched, rows, fp8=False):
     return layer_flops, layer_bytes, {"expert_mlp": mlp}
 
 
-def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=True, experts_fp8=None):
-    """Times beam_moe_forward (or, given experts_fp8, beam_moe_forward_fp8) on the workload."""
+def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=True, experts_fp8=None,
+            experts_fp4=None):
+    """Times beam_moe_forward (or, given experts_fp8 / experts_fp4, beam_moe_forward_fp8 /
+    beam_moe_forward_nvfp4) on the workload."""
     x, wr, b, (wg, wu, wd) = make_layer(shape, T, hot, device, experts)
     out = torch.empty((T, shape.d), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.current_stream()
@@ -159,9 +167,12 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     n_touched = int(torch.unique(idx).numel())
     rows = T * shape.top_k
     fp8 = experts_fp8 is not None
+    fp4 = experts_fp4 is not None
 
     def step():
-        if fp8:
+        if fp4:
+            moe.forward_nvfp4(x, wr, b, experts_fp4, shape, out=out, stream=stream)
+        elif fp8:
             moe.forward_fp8(x, wr, b, experts_fp8, shape, out=out, stream=stream)
         else:
             moe.forward(x, wr, b, wg, wu, wd, shape, out=out, stream=stream)
@@ -203,7 +214,7 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     abi.beam_moe_timing_enable(False)
     stage_ms = {k: v / n2 for k, v in stage_sum.items()}
 
-    layer_flops, layer_bytes, kern = algorithmic(shape, T, n_touched, rows, fp8)
+    layer_flops, layer_bytes, kern = algorithmic(shape, T, n_touched, rows, fp8, fp4)
     t_roof_s = max(layer_flops / (pk["bf16_tflops"] * 1e12), layer_bytes / (pk["hbm_gbs"] * 1e9))
     ms_per_step = total_ms / steps
     dom = "expert_mlp"
@@ -218,7 +229,7 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     roof["kernel"] = dom
     roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
     roof["kernel_ms"] = stage_ms[dom]
-    roof["traffic"] = TRAFFIC.get((name, fp8)) if shape.n_group == 8 else None
+    roof["traffic"] = TRAFFIC.get((name, fp8)) if shape.n_group == 8 and not fp4 else None
     roof["frac_of_sustained"] = (kf / t_dom / 1e12 / pk["bf16_tflops_sustained"]) if not hbm_bound else None
 
     res = {
@@ -375,7 +386,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-tokens", type=int, default=None)
     ap.add_argument("--n-group", type=int, default=8, help="expert groups of 32 (8 = Beam); fewer for profiling")
-    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"], help="expert weights of the headline")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8", "nvfp4"], help="expert weights of the headline")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the token-count sweep T in {1, 8, 64, 256, 1024, 4096, 16384} (BF16)")
     args = ap.parse_args()
@@ -420,9 +431,10 @@ def main():
     torch.cuda.synchronize()
 
     head_fp8 = W.make_experts_fp8(shape, 0, device) if args.weights == "fp8" else None
-    res = measure(name, shape, T, hot, args.steps, args.warmup, experts, device, flush, pk, e2e=head_fp8 is None,
-                  experts_fp8=head_fp8)
-    del head_fp8
+    head_fp4 = W.make_experts_nvfp4(shape, 0, device) if args.weights == "nvfp4" else None
+    res = measure(name, shape, T, hot, args.steps, args.warmup, experts, device, flush, pk,
+                  e2e=head_fp8 is None and head_fp4 is None, experts_fp8=head_fp8, experts_fp4=head_fp4)
+    del head_fp8, head_fp4
     secondary = None
     if not args.no_secondary and name == "decode" and args.n_group == 8 and args.weights == "bf16":
         s_name, s_shape, s_T, s_hot = workload("prefill")
@@ -449,6 +461,20 @@ def main():
                         experts_fp8=experts_fp8)
             fp8[f_name] = summary(f"Beam {f_name} T={f_T}, FP8 E4M3 experts (per-row FP32 scales)", r, f_steps)
         del experts_fp8
+
+    fp4 = None
+    if not args.no_secondary and name == "decode" and args.n_group == 8 and args.weights == "bf16":
+        # The block on NVFP4 expert weights (same draws, quantised): decode and prefill.
+        experts_fp4 = W.make_experts_nvfp4(shape, 0, device)
+        fp4 = {}
+        for f_name in ("decode", "prefill"):
+            f_name, f_shape, f_T, f_hot = workload(f_name)
+            f_steps = args.steps if f_name == "decode" else max(10, min(args.steps, 50))
+            r = measure(f_name, f_shape, f_T, f_hot, f_steps, args.warmup, experts, device, flush, pk, e2e=False,
+                        experts_fp4=experts_fp4)
+            fp4[f_name] = summary(f"Beam {f_name} T={f_T}, NVFP4 experts (E2M1, E4M3 block scales per 16, FP32 "
+                                  f"tensor scale)", r, f_steps)
+        del experts_fp4
 
     sweep = None
     if not args.no_sweep and not args.no_secondary and args.n_group == 8 and args.weights == "bf16":
@@ -486,7 +512,8 @@ def main():
                        "topk_group": shape.topk_group, "top_k": shape.top_k, "scale": shape.scale,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "flushed (512 MB write) before every timed step",
-                       "expert_weights": "BF16" if args.weights == "bf16" else "FP8 E4M3, per-row FP32 scales"},
+                       "expert_weights": {"bf16": "BF16", "fp8": "FP8 E4M3, per-row FP32 scales",
+                                          "nvfp4": "NVFP4 (E2M1, E4M3 block scales, FP32 tensor scale)"}[args.weights]},
             "roofline": {**res["roofline"],
                          "peak_source": (f"measured (MEASURED_PEAKS.json "
                                          f"{'hbm_gbs, copy' if res['roofline']['bound'] == 'hbm' else 'bf16_tflops, burst'})")
@@ -505,6 +532,8 @@ def main():
             line["skewed"] = skewed
         if fp8:
             line["fp8_experts"] = fp8
+        if fp4:
+            line["nvfp4_experts"] = fp4
         if sweep:
             line["sweep"] = sweep
         print(json.dumps(line), flush=True)

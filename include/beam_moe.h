@@ -131,15 +131,37 @@ BEAM_MOE_API int beam_moe_forward_host(const beam_moe_config *cfg, const __nv_bf
  *   Wu[e][i][j] = up_scale[e][i]   * e4m3(w_up_q[e][i][j])        gate_scale, up_scale f32 [E, I]
  *   Wd[e][j][i] = down_scale[e][j] * e4m3(w_down_q[e][j][i])      w_down_q u8 [E, d, I], down_scale f32 [E, d]
  * and otherwise the block of beam_moe_forward_ex: same routing, activations and output in
- * BF16. Numerics: the codes are widened to BF16 exactly on chip, the products run on the
- * BF16 tensor cores with FP32 accumulation, and each accumulator is multiplied by its row's
- * scale in FP32 before SwiGLU (gate/up) or before rounding the expert output (down). All
- * pointers are device memory, 16-byte aligned, owned by the caller and only read (out is
- * written); errors as for beam_moe_forward_ex. */
+ * BF16. Numerics: the products run on the FP8 tensor cores with the codes as they are and
+ * FP32 accumulation; each BF16 activation row (x, and h after its BF16 rounding) enters
+ * them as two E4M3 pieces under one power-of-two row scale s, v = s p1 + (s/16) p2, which is
+ * exact for every value within 2^-10 of the row's largest magnitude (smaller ones carry an
+ * absolute error below 2^-22 of it); each accumulator is multiplied by its row's scale in
+ * FP32 before SwiGLU (gate/up) or before rounding the expert output (down). All pointers are
+ * device memory, 16-byte aligned, owned by the caller and only read (out is written); errors
+ * as for beam_moe_forward_ex. */
 BEAM_MOE_API int beam_moe_forward_fp8(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
                          const float *expert_bias, const uint8_t *w_gate_q, const float *gate_scale,
                          const uint8_t *w_up_q, const float *up_scale, const uint8_t *w_down_q,
                          const float *down_scale, int T, __nv_bfloat16 *out, cudaStream_t stream);
+
+/* Whole MoE block with NVFP4 expert weights. The pages ship an NVFP4 checkpoint of about 4.5
+ * bits per weight for Blackwell GPUs (Glonce "Reflection releases Beam ...", Hardware
+ * paragraph; Atech "Reflection ... Beam ...", checkpoint sizes) but give no layout; this call
+ * takes the public NVFP4 layout as the reading: E2M1 codes (bit 3 sign, 2 exponent bits with
+ * bias 1, 1 mantissa bit) packed two per byte, element 2k in the low half of byte k; one E4M3
+ * scale per block of 16 consecutive elements of a row; one FP32 scale per expert matrix:
+ *   Wg[e][i][j] = gate_tensor_scale[e] * e4m3(gate_block_scale[e][i][j/16]) * e2m1(code j of row i)
+ *   w_gate_q, w_up_q u8 [E, I, d/2]; gate_block_scale, up_block_scale u8 [E, I, d/16]
+ *   w_down_q u8 [E, d, I/2]; down_block_scale u8 [E, d, I/16]; *_tensor_scale f32 [E]
+ * and otherwise the block of beam_moe_forward_ex (same routing, BF16 activations and
+ * output). Numerics: the weights are widened exactly to BF16 on chip and multiplied on the
+ * BF16 tensor cores with FP32 accumulation; the tensor scale is applied to each accumulator.
+ * d and I must be multiples of 256. Pointers as for beam_moe_forward_fp8. */
+BEAM_MOE_API int beam_moe_forward_nvfp4(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
+                           const float *expert_bias, const uint8_t *w_gate_q, const uint8_t *gate_block_scale,
+                           const float *gate_tensor_scale, const uint8_t *w_up_q, const uint8_t *up_block_scale,
+                           const float *up_tensor_scale, const uint8_t *w_down_q, const uint8_t *down_block_scale,
+                           const float *down_tensor_scale, int T, __nv_bfloat16 *out, cudaStream_t stream);
 
 /* One expert-parallel shard of the MoE block. The pages' multi-GPU plan puts each expert on
  * one device and replicates the rest, with a device count that divides 256 (Glonce "Reflection

@@ -34,7 +34,7 @@ EXPORTS = ("beam_moe_default_config", "beam_moe_route", "beam_moe_route_ex", "be
            "beam_moe_route_noalloc", "beam_moe_rmsnorm", "beam_moe_sublayer_forward", "beam_moe_forward_shard",
            "beam_moe_dense_mlp", "beam_moe_forward_fp8", "beam_moe_selftest_wait_timeout",
            "beam_moe_route_noalloc_plan", "beam_moe_route_noalloc_status", "beam_moe_route_noalloc_selftest",
-           "beam_moe_forward_host", "beam_moe_debug_poison_scratch")
+           "beam_moe_forward_host", "beam_moe_debug_poison_scratch", "beam_moe_forward_nvfp4")
 
 
 class BeamMoeConfig(ctypes.Structure):
@@ -85,6 +85,7 @@ def load() -> ctypes.CDLL:
             L.beam_moe_forward_shard.argtypes = [cfgp, P, P, P, P, P, P, i, i, i, P, P]
             L.beam_moe_dense_mlp.argtypes = [i, i, P, P, P, P, i, P, P]
             L.beam_moe_forward_fp8.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i, P, P]
+            L.beam_moe_forward_nvfp4.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, i, P, P]
             L.beam_moe_selftest_wait_timeout.argtypes = [P]
             L.beam_moe_last_error.restype = ctypes.c_char_p
             L.beam_moe_last_error.argtypes = []
@@ -99,7 +100,7 @@ def load() -> ctypes.CDLL:
                       "beam_moe_rmsnorm", "beam_moe_sublayer_forward", "beam_moe_forward_shard",
                       "beam_moe_dense_mlp", "beam_moe_forward_fp8", "beam_moe_selftest_wait_timeout",
            "beam_moe_route_noalloc_plan", "beam_moe_route_noalloc_status", "beam_moe_route_noalloc_selftest",
-           "beam_moe_forward_host", "beam_moe_debug_poison_scratch"):
+           "beam_moe_forward_host", "beam_moe_debug_poison_scratch", "beam_moe_forward_nvfp4"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -204,6 +205,15 @@ def beam_moe_forward_fp8(cfg, x, router_w, expert_bias, w_gate_q, gate_scale, w_
     return _check(load().beam_moe_forward_fp8(_cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate_q),
                                               _ptr(gate_scale), _ptr(w_up_q), _ptr(up_scale), _ptr(w_down_q),
                                               _ptr(down_scale), int(T), _ptr(out), _stream(stream)))
+
+
+def beam_moe_forward_nvfp4(cfg, x, router_w, expert_bias, w_gate_q, gate_block_scale, gate_tensor_scale, w_up_q,
+                           up_block_scale, up_tensor_scale, w_down_q, down_block_scale, down_tensor_scale, T, out,
+                           stream=None):
+    return _check(load().beam_moe_forward_nvfp4(
+        _cfg(cfg), _ptr(x), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate_q), _ptr(gate_block_scale),
+        _ptr(gate_tensor_scale), _ptr(w_up_q), _ptr(up_block_scale), _ptr(up_tensor_scale), _ptr(w_down_q),
+        _ptr(down_block_scale), _ptr(down_tensor_scale), int(T), _ptr(out), _stream(stream)))
 
 
 def beam_moe_selftest_wait_timeout(stream=None):

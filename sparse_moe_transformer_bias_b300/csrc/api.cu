@@ -255,11 +255,12 @@ struct ShardArgs {
 // the residual stream: pre-norm, forward, then combine fused with the post-norm and the
 // residual update into out); 4: forward of one expert-parallel shard (wg/wu/wd hold only
 // experts [e_begin, e_end); FP32 partial output over the slots routed there); 5: forward
-// with FP8 expert weights (q8; wg/wu/wd unused).
+// with FP8 expert weights (q8; wg/wu/wd unused); 6: forward with NVFP4 expert weights (q4;
+// wg/wu/wd unused).
 int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float* bias, const bf16* wg,
         const bf16* wu, const bf16* wd, int T, int32_t* topk_idx, float* topk_w, float* logits, bf16* out, int mode,
         cudaStream_t st, const SublayerArgs* sub = nullptr, const ShardArgs* shard = nullptr,
-        const Fp8Experts* q8 = nullptr) {
+        const Fp8Experts* q8 = nullptr, const Nvfp4Experts* q4 = nullptr) {
     g_launches = 0;
     timing_begin_call();
     int rc;
@@ -275,7 +276,17 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     if (mode != 1 && (rc = check_ptr(bias, "expert_bias"))) return rc;
     if (mode == 0 && ((rc = check_ptr(topk_idx, "topk_idx")) || (rc = check_ptr(topk_w, "topk_w")))) return rc;
     if (mode == 1 && (rc = check_ptr(logits, "logits"))) return rc;
-    if (mode == 5) {
+    if (mode == 6) {
+        if ((rc = check_ptr(q4->wg, "w_gate_q")) || (rc = check_ptr(q4->gbs, "gate_block_scale")) ||
+            (rc = check_ptr(q4->gts, "gate_tensor_scale")) || (rc = check_ptr(q4->wu, "w_up_q")) ||
+            (rc = check_ptr(q4->ubs, "up_block_scale")) || (rc = check_ptr(q4->uts, "up_tensor_scale")) ||
+            (rc = check_ptr(q4->wd, "w_down_q")) || (rc = check_ptr(q4->dbs, "down_block_scale")) ||
+            (rc = check_ptr(q4->dts, "down_tensor_scale")))
+            return rc;
+        if (cfg->d % 256 || cfg->I % 256)
+            return fail(BEAM_MOE_ERR_ARG, "NVFP4 experts need d and I to be multiples of 256 (d=%d, I=%d)", cfg->d,
+                        cfg->I);
+    } else if (mode == 5) {
         if ((rc = check_ptr(q8->wg, "w_gate_q")) || (rc = check_ptr(q8->gs, "gate_scale")) ||
             (rc = check_ptr(q8->wu, "w_up_q")) || (rc = check_ptr(q8->us, "up_scale")) ||
             (rc = check_ptr(q8->wd, "w_down_q")) || (rc = check_ptr(q8->ds, "down_scale")))
@@ -323,7 +334,7 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     Shape se = s;
     se.E = mode == 4 ? shard->e_end - shard->e_begin : s.E;
     const RouterPlan plan = router_plan(s, T, dev->num_sms);
-    const int bn_max = mode == 5 ? gemm_bn_max_f8(s, T) : gemm_bn_max(s, T);
+    const int bn_max = mode == 5 ? gemm_bn_max_f8(s, T) : mode == 6 ? gemm_bn_max_fp4(s, T) : gemm_bn_max(s, T);
     const int max_tiles = dispatch_max_tiles(se, T, bn_max);
     const int rows = T * s.top_k;
     Scratch sc;
@@ -376,6 +387,9 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
                                                      sc.perm_src, sc.xmax, sc.amax_h,
                                                      sc.tiles, sc.tile_done, max_tiles, bn_max, sc.h, sc.y,
                                                      dev->status, dev->num_sms, st));
+            } else if (mode == 6) {
+                LAUNCH(kExpert, launch_expert_mlp_nvfp4(se, *q4, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
+                                                        bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
             } else
                 LAUNCH(kExpert, launch_expert_mlp(se, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done,
                                                   max_tiles, bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
@@ -516,6 +530,17 @@ int beam_moe_forward_fp8(const beam_moe_config* cfg, const __nv_bfloat16* x, con
     const Fp8Experts q{w_gate_q, gate_scale, w_up_q, up_scale, w_down_q, down_scale};
     return run(cfg, x, router_w, expert_bias, nullptr, nullptr, nullptr, T, nullptr, nullptr, nullptr, out, 5, stream,
                nullptr, nullptr, &q);
+}
+
+int beam_moe_forward_nvfp4(const beam_moe_config* cfg, const __nv_bfloat16* x, const float* router_w,
+                           const float* expert_bias, const uint8_t* w_gate_q, const uint8_t* gate_block_scale,
+                           const float* gate_tensor_scale, const uint8_t* w_up_q, const uint8_t* up_block_scale,
+                           const float* up_tensor_scale, const uint8_t* w_down_q, const uint8_t* down_block_scale,
+                           const float* down_tensor_scale, int T, __nv_bfloat16* out, cudaStream_t stream) {
+    const Nvfp4Experts q{w_gate_q,       gate_block_scale, gate_tensor_scale, w_up_q,           up_block_scale,
+                         up_tensor_scale, w_down_q,        down_block_scale,  down_tensor_scale};
+    return run(cfg, x, router_w, expert_bias, nullptr, nullptr, nullptr, T, nullptr, nullptr, nullptr, out, 6, stream,
+               nullptr, nullptr, nullptr, &q);
 }
 
 int beam_moe_dense_mlp(int d, int I, const __nv_bfloat16* x, const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up,

@@ -128,14 +128,30 @@ struct Fp8Experts {
     const uint8_t* wd;
     const float* ds;
 };
-// Largest N-tile of the FP8 expert kernel (its converted weights share TMEM with the
-// accumulators, so tiles stop at 192 rows).
-int gemm_bn_max_fp8(const Shape& s, int T);
-// The expert kernel on FP8 weights: the same items and outputs as launch_expert_mlp, the
-// weight tiles widened to BF16 on chip and the accumulators scaled per weight row.
-cudaError_t launch_expert_mlp_fp8(const Shape& s, const Fp8Experts& q, const bf16* x_perm, int rows,
-                                  const int4* tiles, int* tile_done, int max_tiles, int bn_max, bf16* h, bf16* y,
-                                  int* status, int num_sms, cudaStream_t st);
+// NVFP4 expert weights: E2M1 codes packed two per byte (element 2k in the low half of byte
+// k), one E4M3 block scale per 16 elements of a row, one FP32 tensor scale per expert
+// matrix: W[r][c] = ts * e4m3(bs[r][c / 16]) * e2m1(code c of row r).
+// wg, wu [E, I, d/2] with gbs, ubs [E, I, d/16] and gts, uts [E]; wd [E, d, I/2] with dbs
+// [E, d, I/16] and dts [E].
+struct Nvfp4Experts {
+    const uint8_t* wg;
+    const uint8_t* gbs;
+    const float* gts;
+    const uint8_t* wu;
+    const uint8_t* ubs;
+    const float* uts;
+    const uint8_t* wd;
+    const uint8_t* dbs;
+    const float* dts;
+};
+// Largest N-tile of the NVFP4 expert kernel (its widened weights share TMEM with the
+// accumulators, so tiles stop at 128 rows).
+int gemm_bn_max_fp4(const Shape& s, int T);
+// The expert kernel on NVFP4 weights (expert_mlp.cu): the same items and outputs as
+// launch_expert_mlp, the weights widened exactly to BF16 on chip; d and I multiples of 256.
+cudaError_t launch_expert_mlp_nvfp4(const Shape& s, const Nvfp4Experts& q, const bf16* x_perm, int rows,
+                                    const int4* tiles, int* tile_done, int max_tiles, int bn_max, bf16* h, bf16* y,
+                                    int* status, int num_sms, cudaStream_t st);
 // FP8 E4M3 expert weights on the FP8 tensor cores (expert_mlp_fp8.cu): the same items and
 // outputs as launch_expert_mlp. Activations enter the products as two E4M3 pieces per row
 // under a power-of-two row scale: x8_perm holds the dispatched pieces of x (per permuted
@@ -218,5 +234,8 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint
 // 128-byte-wide box sits at chunk c ^ (r & 7).
 bool encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                        uint32_t box_cols, const char** why);
+// The same without swizzle (rows of box_cols bytes one after another in shared memory).
+bool encode_tmap_u8_2d_plain(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                             uint32_t box_cols, const char** why);
 
 }  // namespace beam

@@ -37,6 +37,7 @@ struct CachedMap {
     const void* base;
     uint64_t rows, cols, row_bytes;
     uint32_t box_rows, box_cols;
+    CUtensorMapSwizzle swizzle;
     CUtensorMap map;
 };
 constexpr int kCacheEntries = 64;
@@ -44,10 +45,11 @@ thread_local CachedMap g_cache[kCacheEntries];
 thread_local int g_cache_next = 0;
 
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t rows, uint64_t cols,
-               uint64_t row_bytes, uint32_t box_rows, uint32_t box_cols, const char** why) {
+               uint64_t row_bytes, uint32_t box_rows, uint32_t box_cols, const char** why,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     for (const CachedMap& c : g_cache) {
         if (c.used && c.dtype == dtype && c.base == base && c.rows == rows && c.cols == cols &&
-            c.row_bytes == row_bytes && c.box_rows == box_rows && c.box_cols == box_cols) {
+            c.row_bytes == row_bytes && c.box_rows == box_rows && c.box_cols == box_cols && c.swizzle == swizzle) {
             *map = c.map;
             return true;
         }
@@ -62,8 +64,8 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *why = "cuTensorMapEncodeTiled rejected a tensor map";
         return false;
@@ -78,6 +80,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
     c.row_bytes = row_bytes;
     c.box_rows = box_rows;
     c.box_cols = box_cols;
+    c.swizzle = swizzle;
     c.map = *map;
     return true;
 }
@@ -104,6 +107,12 @@ bool encode_bmaps(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int 
         if (!encode_tmap_bf16_2d(&b->m[i], base, rows, cols, h, kTileK, why)) return false;
     }
     return true;
+}
+
+bool encode_tmap_u8_2d_plain(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                             uint32_t box_cols, const char** why) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rows, cols, cols, box_rows, box_cols, why,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool encode_bmaps_u8(BMaps* b, const void* base, uint64_t rows, uint64_t cols, int box_max, const char** why) {

@@ -68,6 +68,23 @@ def forward_fp8(x, router_w, bias, experts_fp8, shape: MoEShape = BEAM, out=None
     return out
 
 
+def forward_nvfp4(x, router_w, bias, experts_nvfp4, shape: MoEShape = BEAM, out=None, stream=None):
+    """The block with NVFP4 expert weights: experts_nvfp4 = ((wg_q, wg_bs, wg_t), (wu_q, wu_bs, wu_t),
+    (wd_q, wd_bs, wd_t)) with codes uint8 [E, rows, cols/2], E4M3 block scales uint8
+    [E, rows, cols/16] and FP32 tensor scales [E] (workloads.make_experts_nvfp4 builds them)."""
+    T = _check_inputs(shape, x, router_w, bias)
+    parts = []
+    for (q, bs, t), rows, cols in zip(experts_nvfp4, (shape.I, shape.I, shape.d), (shape.d, shape.d, shape.I)):
+        assert q.dtype == torch.uint8 and q.shape == (shape.E, rows, cols // 2) and q.is_contiguous()
+        assert bs.dtype == torch.uint8 and bs.shape == (shape.E, rows, cols // 16) and bs.is_contiguous()
+        assert t.dtype == torch.float32 and t.shape == (shape.E,) and t.is_contiguous()
+        parts += [q, bs, t]
+    if out is None:
+        out = torch.empty((T, shape.d), dtype=torch.bfloat16, device=x.device)
+    abi.beam_moe_forward_nvfp4(shape, x, router_w, bias, *parts, T, out, stream)
+    return out
+
+
 def forward_host(x_host, router_w, bias, w_gate, w_up, w_down, shape: MoEShape = BEAM, out_host=None, stream=None):
     """Host tokens in, host output out, in one library call (beam_moe_forward_host): the copy
     of x to the device, the block and the copy of the output back, on `stream`; returns

@@ -1,0 +1,152 @@
+"""NVFP4 expert weights: the CUDA block with E2M1 codes, E4M3 block scales and FP32 tensor
+scales against the oracle on the same codes and scales (forward_nvfp4), element by
+element, on Tiny (every token, ragged counts, both N-tile sizes of the NVFP4 kernel: 32 rows
+for T <= 32, else 128) and on Beam shapes (sampled tokens at full size), plus a case that
+puts every E2M1 code and a wide range of block scales through the on-chip widening."""
+import numpy as np
+import pytest
+import torch
+
+import parity as P
+from oracle import oracle as O
+from sparse_moe_transformer_bias_b300 import abi, moe, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def host_experts(q4, cache=None):
+    """Oracle callable e -> (gate, up, down), each (codes, block scales, tensor scale), over
+    device NVFP4 experts, copying an expert to the host on first use."""
+    cache = {} if cache is None else cache
+
+    def get(e):
+        if e not in cache:
+            cache[e] = tuple((q[e].cpu().numpy(), bs[e].cpu().numpy(), float(t[e])) for q, bs, t in q4)
+        return cache[e]
+    return get
+
+
+def run_and_check(shape, x, wr, b, q4, tokens, what, cache=None):
+    out = moe.forward_nvfp4(x, wr, b, q4, shape)
+    logits = moe.router_logits(x, wr, shape).cpu().numpy()
+    idx, _ = moe.route(x, wr, b, shape)
+    abi.beam_moe_device_status()
+    out = out.float().cpu().numpy()
+    tokens = np.asarray(tokens, np.int64)
+    bh = b.cpu().numpy()
+    _, _, dbg = O.route(shape, logits[tokens], bh, debug=True)
+    flagged = P.near_tie_tokens(shape, dbg)
+    experts = host_experts(q4, cache)
+    ref, _ = O.forward_nvfp4(shape, O.bf16_bits(x), bh, experts, tokens, logits=logits)
+    if len(flagged):
+        ref2, _ = O.forward_nvfp4(shape, O.bf16_bits(x), bh, experts, tokens[flagged], logits=logits,
+                                  idx_in=idx.cpu().numpy()[tokens[flagged]])
+        ref[flagged] = ref2
+    frob = P.check_output(out[tokens], ref, what)
+    print(f"{what}: tokens checked {len(tokens)}, near-tie {len(flagged)}, rel frob {frob:.2e}")
+    return out
+
+
+@pytest.fixture(scope="module")
+def tiny_fp4():
+    return W.make_experts_nvfp4(W.TINY, seed=0, device="cuda")
+
+
+@pytest.mark.parametrize("T", [1, 16, 33, 129, 300, 1500])
+def test_tiny_nvfp4_parity(tiny_fp4, T):
+    shape = W.TINY
+    x = W.make_tokens(shape, T, 0, "cuda")
+    wr, b = W.make_router(shape, 0, "cuda")
+    run_and_check(shape, x, wr, b, tiny_fp4, np.arange(T), f"tiny nvfp4 T={T}")
+
+
+def test_every_code_and_a_wide_range_of_block_scales():
+    """Codes cycle through all 16 E2M1 values and block scales cover the E4M3 codes from the
+    subnormal 2^-9 to 448; tensor scales are powers of two, so every dequantised weight is an
+    exact BF16 value (a product of 2, 4 and 1 significant bits). The widening must be exact:
+    the NVFP4 block must give what the BF16 block gives on those BF16 weights (the same MMAs
+    in the same order; only powers of two differ), and both must match the oracle to the
+    output tolerance's Frobenius bound row by row. (Block scales 2^18 apart make some
+    outputs cancel far below their terms, where the BF16 rounding of h, common to both
+    blocks, exceeds the per-element bound.)"""
+    import pins
+    shape = W.TINY
+    E, d, I = shape.E, shape.d, shape.I
+    gen = torch.Generator().manual_seed(17)
+
+    def part(rows, cols):
+        q = torch.randint(0, 256, (E, rows, cols // 2), generator=gen, dtype=torch.int32).to(torch.uint8)
+        bs = torch.randint(1, 127, (E, rows, cols // 16), generator=gen, dtype=torch.int32).to(torch.uint8)
+        t = torch.full((E,), 2.0 ** -10, dtype=torch.float32)
+        return q, bs, t
+
+    parts = (part(I, d), part(I, d), part(d, I))
+    deq = [torch.stack([pins.nvfp4_dequant_torch(q[e], bs[e], t[e]) for e in range(E)]) for q, bs, t in parts]
+    wbf = [w.to(torch.bfloat16) for w in deq]
+    for w, wb in zip(deq, wbf):
+        assert torch.equal(wb.double(), w)
+    q4 = tuple((q.cuda(), bs.cuda(), t.cuda()) for q, bs, t in parts)
+    T = 40
+    x = W.make_tokens(shape, T, 4, "cuda")
+    wr, b = W.make_router(shape, 4, "cuda")
+    o4 = moe.forward_nvfp4(x, wr, b, q4, shape).double().cpu().numpy()
+    o16 = moe.forward(x, wr, b, *(w.cuda() for w in wbf), shape).double().cpu().numpy()
+    logits = moe.router_logits(x, wr, shape).cpu().numpy()
+    abi.beam_moe_device_status()
+    np.testing.assert_array_equal(o4, o16)
+    experts = lambda e: (O.bf16_bits(wbf[0][e]), O.bf16_bits(wbf[1][e]), O.bf16_bits(wbf[2][e]))  # noqa: E731
+    ref, _, _ = O.forward(shape, O.bf16_bits(x), b.cpu().numpy(), experts, logits=logits)
+    for t in range(T):
+        assert np.linalg.norm(o4[t] - ref[t]) <= P.FROB * np.linalg.norm(ref[t]), t
+
+
+def test_nvfp4_deterministic(tiny_fp4):
+    shape = W.TINY
+    x = W.make_tokens(shape, 300, 7, "cuda")
+    wr, b = W.make_router(shape, 7, "cuda")
+    a = moe.forward_nvfp4(x, wr, b, tiny_fp4, shape)
+    c = moe.forward_nvfp4(x, wr, b, tiny_fp4, shape)
+    torch.cuda.synchronize()
+    assert torch.equal(a, c)
+
+
+def test_nvfp4_close_to_bf16_block(tiny_fp4):
+    """Same draws as the BF16 experts, quantised to NVFP4: the blocks differ by the
+    quantisation error (about 10% relative per weight, averaging out over the sums)."""
+    shape = W.TINY
+    x = W.make_tokens(shape, 200, 1, "cuda")
+    wr, b = W.make_router(shape, 1, "cuda")
+    wg, wu, wd = W.make_experts(shape, 0, "cuda")
+    ref = moe.forward(x, wr, b, wg, wu, wd, shape).double()
+    got = moe.forward_nvfp4(x, wr, b, tiny_fp4, shape).double()
+    rel = float((got - ref).norm() / ref.norm())
+    assert rel < 0.2, rel
+
+
+def test_nvfp4_rejects_shapes_off_the_block_grid():
+    shape = W.MoEShape(d=384, I=256)
+    x = torch.zeros((4, shape.d), dtype=torch.bfloat16, device="cuda")
+    wr, b = W.make_router(shape, 0, "cuda")
+    q4 = tuple((torch.zeros((shape.E, r, c // 2), dtype=torch.uint8, device="cuda"),
+                torch.zeros((shape.E, r, c // 16), dtype=torch.uint8, device="cuda"),
+                torch.ones((shape.E,), dtype=torch.float32, device="cuda"))
+               for r, c in ((shape.I, shape.d), (shape.I, shape.d), (shape.d, shape.I)))
+    with pytest.raises(abi.BeamMoeError) as err:
+        moe.forward_nvfp4(x, wr, b, q4, shape)
+    assert err.value.code == abi.BEAM_MOE_ERR_ARG and "multiples of 256" in str(err.value)
+
+
+@pytest.fixture(scope="module")
+def beam_fp4():
+    return W.make_experts_nvfp4(W.BEAM, seed=0, device="cuda")
+
+
+@pytest.mark.parametrize("name,T,n_check", [("decode", 16, 16), ("prefill", 4096, 8)])
+def test_beam_nvfp4_parity(beam_fp4, name, T, n_check):
+    shape = W.BEAM
+    x = W.make_tokens(shape, T, 0, "cuda")
+    wr, b = W.make_router(shape, 0, "cuda")
+    tokens = W.sample_tokens(T, n_check, seed=2).numpy()
+    if T > n_check:
+        tokens = np.unique(np.concatenate([tokens, [T - 1]]))
+    run_and_check(shape, x, wr, b, beam_fp4, tokens, f"{name} nvfp4 T={T}")
