@@ -43,11 +43,16 @@ METRIC = "Beam MoE-layer tokens/s (T=16 decode, T=4096 prefill); % of roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes (read + write) of one launch of the dominant kernel on the bench's own
-# full-size workloads (seeded, so every run routes the same way), from one-pass ncu
-# captures of dram__bytes_read.sum and dram__bytes_write.sum; remove an entry when its
-# kernel changes after the capture. Keys: (workload name, FP8 experts).
-TRAFFIC = {("decode", False): 7000938240 + 4401408, ("prefill", False): 19823741440 + 495698688}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the expert
+# kernel over its algorithmic bytes, from one-launch ncu captures of the same kernels on the
+# same workloads with one group of 32 experts (the size a capture may hold): decode T=16 and
+# the prefill-shaped T=512 (128 rows per expert, as at T=4096 with 256 experts). The bench
+# scales its own algorithmic bytes by these ratios (the traffic is the touched experts'
+# weights plus the activations, both in proportion). Keys: (workload, weights); remove an
+# entry when its kernel changes after the capture.
+TRAFFIC_RATIO = {("decode", "bf16"): 2521634560 / 2520514560, ("prefill", "bf16"): 2607164672 / 2642411520,
+                 ("decode", "fp8"): 1266699776 / 1263534080, ("prefill", "fp8"): 1472596224 / 1385431040,
+                 ("decode", "nvfp4"): 716948736 / 711721344, ("prefill", "nvfp4"): 955522560 / 833618304}
 
 
 def peaks():
@@ -229,7 +234,8 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     roof["kernel"] = dom
     roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
     roof["kernel_ms"] = stage_ms[dom]
-    roof["traffic"] = TRAFFIC.get((name, fp8)) if shape.n_group == 8 and not fp4 else None
+    ratio = TRAFFIC_RATIO.get((name, "nvfp4" if fp4 else "fp8" if fp8 else "bf16"))
+    roof["traffic"] = int(ratio * kb) if ratio is not None and shape.n_group == 8 else None
     roof["frac_of_sustained"] = (kf / t_dom / 1e12 / pk["bf16_tflops_sustained"]) if not hbm_bound else None
 
     res = {
@@ -291,16 +297,19 @@ def measure_e2e(shape, T, x, wr, b, wg, wu, wd, steps, warmup, flush):
     for _ in range(warmup):
         moe.forward_host(x_host, wr, b, wg, wu, wd, shape, out_host=out_host, stream=stream)
     total = 0.0
+    per_step = []
     for _ in range(steps):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         moe.forward_host(x_host, wr, b, wg, wu, wd, shape, out_host=out_host, stream=stream)
-        total += time.perf_counter() - t0
+        per_step.append(time.perf_counter() - t0)
+        total += per_step[-1]
     total = max_over_ranks(total * 1e3) * 1e-3
     res = {"value": T * steps / total, "unit": "tokens/s", "h2d_bytes_per_step": T * shape.d * 2,
            "d2h_bytes_per_step": T * shape.d * 2, "call": "beam_moe_forward_host",
-           "timer": "host wall clock around each synchronous step"}
+           "timer": "host wall clock around each synchronous step",
+           "ms_per_step_p10_p50_p90": [float(np.percentile(per_step, q)) * 1e3 for q in (10, 50, 90)]}
     # The same through moe.ForwardGraph: the call captured once, replayed per step.
     g = moe.ForwardGraph(x_dev, wr, b, wg, wu, wd, shape, out=out_dev)
     stream = torch.cuda.current_stream()

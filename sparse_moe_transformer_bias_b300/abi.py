@@ -46,6 +46,9 @@ class BeamMoeConfig(ctypes.Structure):
         return cls(shape.d, shape.I, shape.E, shape.n_group, shape.topk_group, shape.top_k, float(shape.scale))
 
 
+_cfg_cache = {}
+
+
 class BeamMoeError(RuntimeError):
     def __init__(self, code: int, message: str):
         super().__init__(f"beam_moe error {code}: {message}")
@@ -132,7 +135,12 @@ def _check(rc: int):
 def _cfg(cfg):
     if cfg is None:
         return None
-    return ctypes.byref(cfg if isinstance(cfg, BeamMoeConfig) else BeamMoeConfig.of(cfg))
+    if isinstance(cfg, BeamMoeConfig):
+        return ctypes.byref(cfg)
+    c = _cfg_cache.get(cfg)  # shapes are frozen dataclasses: one struct per shape
+    if c is None:
+        c = _cfg_cache.setdefault(cfg, BeamMoeConfig.of(cfg))
+    return ctypes.byref(c)
 
 
 def beam_moe_default_config() -> BeamMoeConfig:
