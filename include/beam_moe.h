@@ -154,9 +154,15 @@ BEAM_MOE_API int beam_moe_forward_fp8(const beam_moe_config *cfg, const __nv_bfl
  *   w_gate_q, w_up_q u8 [E, I, d/2]; gate_block_scale, up_block_scale u8 [E, I, d/16]
  *   w_down_q u8 [E, d, I/2]; down_block_scale u8 [E, d, I/16]; *_tensor_scale f32 [E]
  * and otherwise the block of beam_moe_forward_ex (same routing, BF16 activations and
- * output). Numerics: the weights are widened exactly to BF16 on chip and multiplied on the
- * BF16 tensor cores with FP32 accumulation; the tensor scale is applied to each accumulator.
- * d and I must be multiples of 256. Pointers as for beam_moe_forward_fp8. */
+ * output). Numerics: the products run on the block-scaled FP4 tensor cores with the codes
+ * and block scales as they are and FP32 accumulation. Each activation row (x, and h in FP32
+ * straight from SwiGLU) enters them as four NVFP4 pieces: per block of 16 elements, piece p
+ * has the E4M3 scale u_p = the least E4M3 value >= 2^(3p) max|r_p| / 6 and the E2M1 codes of
+ * r_p / (2^-3p u_p) rounded to nearest, r_0 = v, r_(p+1) = r_p - 2^-3p u_p e2m1(code); what
+ * is left after four pieces is at most 1.2e-3 of the block's largest magnitude. The tensor
+ * scale is applied to each accumulator. A block whose largest magnitude exceeds 2688 is
+ * clamped and recorded in the device status word (code 4). d and I must be multiples of 256.
+ * Pointers as for beam_moe_forward_fp8. */
 BEAM_MOE_API int beam_moe_forward_nvfp4(const beam_moe_config *cfg, const __nv_bfloat16 *x, const float *router_w,
                            const float *expert_bias, const uint8_t *w_gate_q, const uint8_t *gate_block_scale,
                            const float *gate_tensor_scale, const uint8_t *w_up_q, const uint8_t *up_block_scale,
@@ -280,7 +286,8 @@ BEAM_MOE_API const char *beam_moe_last_error(void);
 /* Synchronises `stream`, then returns and clears the current device's kernel status word:
  * 0 if no kernel recorded an error since the last call, else BEAM_MOE_ERR_DEVICE (the
  * message names the recorded code: 1 = an expert index out of range reached dispatch,
- * 2 = a pipeline wait in a GEMM ran past its limit). */
+ * 2 = a pipeline wait in a GEMM ran past its limit, 3 = a permuted row or work-list index
+ * out of range, 4 = an activation block of the NVFP4 block above 2688 in magnitude). */
 BEAM_MOE_API int beam_moe_device_status(cudaStream_t stream);
 
 /* Self-test of failure detection (no counterpart on the pages). Runs the expert kernel on a
@@ -298,8 +305,8 @@ BEAM_MOE_API int beam_moe_selftest_wait_timeout(cudaStream_t stream);
  * on the last call's final event and writes up to max_stages durations in milliseconds
  * (stage order: pre-norm, router weight split, router logits, router select, dispatch count,
  * dispatch scan, dispatch scatter, gather, expert MLP (gate/up, SwiGLU and down in one
- * kernel), combine (fused with the post-norm and residual in beam_moe_sublayer_forward);
- * for T <= 128 the whole dispatch and gather is one launch, timed as dispatch count; unrun
+ * kernel), combine (fused with the post-norm and residual in beam_moe_sublayer_forward),
+ * activation split (the FP8 and NVFP4 blocks' pieces of the token rows); for T <= 128 the whole dispatch and gather is one launch, timed as dispatch count; unrun
  * stages read 0). Returns the number of stages, or a negative error. */
 BEAM_MOE_API int beam_moe_timing_enable(int enable);
 BEAM_MOE_API int beam_moe_timing_read(float *ms, int max_stages);

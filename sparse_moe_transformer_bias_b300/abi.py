@@ -25,7 +25,7 @@ BEAM_MOE_NOALLOC_MAX_TOKENS = 8192
 BEAM_MOE_NOALLOC_SCRATCH_BYTES = 40 << 20
 
 STAGES = ("pre_norm", "router_split", "router_logits", "router_select", "dispatch_count", "dispatch_scan",
-          "dispatch_scatter", "gather", "expert_mlp", "combine", "fp8_prep")
+          "dispatch_scatter", "gather", "expert_mlp", "combine", "act_prep")
 
 # Every symbol include/beam_moe.h declares.
 EXPORTS = ("beam_moe_default_config", "beam_moe_route", "beam_moe_route_ex", "beam_moe_forward",

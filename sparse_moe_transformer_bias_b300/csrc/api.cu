@@ -106,7 +106,7 @@ int check_stream(cudaStream_t st) {
 
 // ---------------------------------------------------------------- stage timing
 enum Stage {
-    kPreNorm, kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kExpert, kCombine, kFp8Prep, kNumStages
+    kPreNorm, kSplitW, kLogits, kSelect, kCount, kScan, kScatter, kGather, kExpert, kCombine, kActPrep, kNumStages
 };
 struct Timing {
     bool enabled = false;
@@ -179,7 +179,10 @@ struct Scratch {
     bf16* y = nullptr;
     float* xmax = nullptr;    // FP8 products: largest |x| per token
     float* amax_h = nullptr;  // FP8 products: largest |h| per permuted row
-    uint8_t* x8 = nullptr;    // FP8 products: the two E4M3 pieces of every token row [T][2][d]
+    uint8_t* x8 = nullptr;    // the pieces of every token row: FP8 [T][2][d], NVFP4 codes [T][4][d/2]
+    uint8_t* xs = nullptr;    // NVFP4 products: block scales of the token rows' pieces [T][4][d/16]
+    uint8_t* xs_perm = nullptr;  // the same for the dispatched rows [rows][4][d/16]
+    uint8_t* hs = nullptr;    // NVFP4 products: block scales of h's pieces [rows][4][I/16]
 };
 
 struct Carver {
@@ -196,7 +199,7 @@ struct Carver {
 
 // Lays scratch out from `base` (nullptr: size only). Returns the byte count.
 size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool forward, bool route_out,
-              bool pre_norm, bool fp8, char* base, Scratch* sc) {
+              bool pre_norm, int pieces, char* base, Scratch* sc) {
     Carver c{base};
     const size_t pairs = static_cast<size_t>(T) * s.top_k;
     sc->x_norm = pre_norm ? c.take<bf16>(static_cast<size_t>(T) * s.d) : nullptr;
@@ -217,10 +220,15 @@ size_t layout(const Shape& s, int T, const RouterPlan& plan, int max_tiles, bool
         sc->x_perm = c.take<bf16>(pairs * s.d);
         sc->h = c.take<bf16>(pairs * s.I);
         sc->y = c.take<bf16>(pairs * s.d);
-        if (fp8) {
+        if (pieces == 2) {
             sc->xmax = c.take<float>(static_cast<size_t>(T));
             sc->amax_h = c.take<float>(pairs);
             sc->x8 = c.take<uint8_t>(static_cast<size_t>(T) * 2 * s.d);
+        } else if (pieces == 4) {
+            sc->x8 = c.take<uint8_t>(static_cast<size_t>(T) * 2 * s.d);
+            sc->xs = c.take<uint8_t>(static_cast<size_t>(T) * s.d / 4);
+            sc->xs_perm = c.take<uint8_t>(pairs * s.d / 4);
+            sc->hs = c.take<uint8_t>(pairs * s.I / 4);
         }
     }
     return c.off + 256;
@@ -334,16 +342,17 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
     Shape se = s;
     se.E = mode == 4 ? shard->e_end - shard->e_begin : s.E;
     const RouterPlan plan = router_plan(s, T, dev->num_sms);
-    const int bn_max = mode == 5 ? gemm_bn_max_f8(s, T) : mode == 6 ? gemm_bn_max_fp4(s, T) : gemm_bn_max(s, T);
+    const int bn_max = mode == 5 ? gemm_bn_max_f8(s, T) : mode == 6 ? gemm_bn_max_nvf4(s, T) : gemm_bn_max(s, T);
+    const int pieces = mode == 5 ? 2 : mode == 6 ? 4 : 0;  // activation pieces of the low-precision products
     const int max_tiles = dispatch_max_tiles(se, T, bn_max);
     const int rows = T * s.top_k;
     Scratch sc;
     const bool fwd = mode >= 2;
-    const size_t bytes = layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, mode == 5, nullptr, &sc);
+    const size_t bytes = layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, pieces, nullptr, &sc);
     void* mem = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&mem, bytes, dev->pool, st);
     if (e != cudaSuccess) return fail(BEAM_MOE_ERR_CUDA, "scratch allocation of %zu bytes: %s", bytes, cudaGetErrorString(e));
-    layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, mode == 5, static_cast<char*>(mem), &sc);
+    layout(s, T, plan, max_tiles, fwd, mode != 0, mode == 3, pieces, static_cast<char*>(mem), &sc);
     if ((e = maybe_poison(mem, bytes, st)) != cudaSuccess) {
         rc = fail(BEAM_MOE_ERR_CUDA, "scratch poison: %s", cudaGetErrorString(e));
         goto done;
@@ -361,18 +370,23 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
         LAUNCH(kSelect, launch_router_select(s, sc.partial, plan.splits, mode == 1 ? nullptr : bias, T, idx, w,
                                              mode == 1 ? logits : nullptr, st));
         if (fwd) {
-            // FP8 products: each token row is split into its two E4M3 pieces first; the
-            // dispatch then moves those rows (2d bytes each, as a BF16 row) instead of x.
+            // FP8 / NVFP4 products: each token row is split into its two E4M3 or four NVFP4
+            // pieces first; the dispatch then moves those rows (2d bytes each, as a BF16 row)
+            // instead of x, and for NVFP4 the pieces' block scales beside them.
             const bf16* rows_src = x;
             if (mode == 5) {
-                LAUNCH(kFp8Prep, launch_fp8_prep(x, s.d, T, sc.xmax, sc.x8, sc.amax_h, rows, dev->num_sms, st));
+                LAUNCH(kActPrep, launch_fp8_prep(x, s.d, T, sc.xmax, sc.x8, sc.amax_h, rows, dev->num_sms, st));
+                rows_src = reinterpret_cast<const bf16*>(sc.x8);
+            } else if (mode == 6) {
+                LAUNCH(kActPrep, launch_act4_prep(x, s.d, T, sc.x8, sc.xs, dev->status, dev->num_sms, st));
                 rows_src = reinterpret_cast<const bf16*>(sc.x8);
             }
+            const int side_bytes = mode == 6 ? s.d / 4 : 0;
             if (T <= kSmallDispatchT) {
                 // one launch for the whole dispatch (timed as the count stage)
                 LAUNCH(kCount, launch_dispatch_small(s, e_lo, se.E, idx, T, bn_max, rows_src, sc.expert_offset, sc.tiles,
                                                      sc.tile_done, sc.perm_src, sc.inv_slot, sc.x_perm, dev->status,
-                                                     dev->num_sms, st));
+                                                     dev->num_sms, st, sc.xs, side_bytes, sc.xs_perm));
             } else {
                 LAUNCH(kCount, launch_dispatch_count(s, e_lo, se.E, idx, T, sc.chunk, dev->status, st));
                 LAUNCH(kScan,
@@ -380,7 +394,7 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
                 LAUNCH(kScatter, launch_dispatch_scatter(s, e_lo, se.E, idx, T, sc.chunk, sc.perm_src, sc.inv_slot,
                                                          dev->status, st));
                 LAUNCH(kGather, launch_gather_rows(rows_src, s.d, T, sc.perm_src, sc.expert_offset + se.E, rows, sc.x_perm,
-                                                   dev->status, dev->num_sms, st));
+                                                   dev->status, dev->num_sms, st, sc.xs, side_bytes, sc.xs_perm));
             }
             if (mode == 5) {
                 LAUNCH(kExpert, launch_expert_mlp_f8(se, *q8, reinterpret_cast<const uint8_t*>(sc.x_perm), rows, T,
@@ -388,8 +402,10 @@ int run(const beam_moe_config* cfg, const bf16* x, const float* wr, const float*
                                                      sc.tiles, sc.tile_done, max_tiles, bn_max, sc.h, sc.y,
                                                      dev->status, dev->num_sms, st));
             } else if (mode == 6) {
-                LAUNCH(kExpert, launch_expert_mlp_nvfp4(se, *q4, sc.x_perm, rows, sc.tiles, sc.tile_done, max_tiles,
-                                                        bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
+                LAUNCH(kExpert, launch_expert_mlp_nvf4(se, *q4, reinterpret_cast<const uint8_t*>(sc.x_perm), sc.xs_perm,
+                                                       rows, sc.tiles, sc.tile_done, max_tiles, bn_max,
+                                                       reinterpret_cast<uint8_t*>(sc.h), sc.hs, sc.y, dev->status,
+                                                       dev->num_sms, st));
             } else
                 LAUNCH(kExpert, launch_expert_mlp(se, wg, wu, wd, sc.x_perm, rows, sc.tiles, sc.tile_done,
                                                   max_tiles, bn_max, sc.h, sc.y, dev->status, dev->num_sms, st));
@@ -676,6 +692,7 @@ int beam_moe_device_status(cudaStream_t stream) {
                 word == kStatusBadExpert    ? "expert index out of range in dispatch"
                 : word == kStatusWaitTimeout ? "a GEMM pipeline wait ran past its limit"
                 : word == kStatusBadIndex    ? "a permuted row or work-list index out of range (access skipped)"
+                : word == kStatusRange       ? "an NVFP4 activation block above 2688 in magnitude (clamped)"
                                              : "unknown");
 }
 

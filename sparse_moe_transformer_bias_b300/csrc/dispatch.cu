@@ -156,23 +156,33 @@ __global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(const int32_t*
     }
 }
 
+// x_perm[row] = x[perm_src[row]] for the dispatched rows, 16 bytes at a time; with a side
+// array (side_vecs > 0) also side_dst[row] = side_src[perm_src[row]] (rows of side_vecs
+// 16-byte pieces: the block scales of the NVFP4 activation pieces).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int row_vecs, int T,
                                                           const int* __restrict__ perm_src,
                                                           const int* __restrict__ n_rows,
-                                                          uint4* __restrict__ x_perm, int* status) {
+                                                          uint4* __restrict__ x_perm, const uint4* __restrict__ side_src,
+                                                          int side_vecs, uint4* __restrict__ side_dst, int* status) {
     pdl_wait();
     pdl_trigger();
-    const size_t total = static_cast<size_t>(*n_rows) * row_vecs;  // rows this call dispatched
+    const size_t n = static_cast<size_t>(*n_rows);  // rows this call dispatched
+    const size_t main_total = n * row_vecs;
+    const size_t total = main_total + n * side_vecs;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const size_t r = i / row_vecs;
-        const size_t v = i - r * row_vecs;
+        const bool side = i >= main_total;
+        const size_t j = side ? i - main_total : i;
+        const int w = side ? side_vecs : row_vecs;
+        const size_t r = j / w;
+        const size_t v = j - r * w;
         const int src = perm_src[r];
         if (static_cast<unsigned>(src) >= static_cast<unsigned>(T)) {
             atomicCAS(status, 0, kStatusBadIndex);
             continue;
         }
-        x_perm[i] = x[static_cast<size_t>(src) * row_vecs + v];
+        if (side) side_dst[j] = side_src[static_cast<size_t>(src) * w + v];
+        else x_perm[j] = x[static_cast<size_t>(src) * w + v];
     }
 }
 
@@ -182,7 +192,8 @@ constexpr int kSmallThreads = 256;  // >= the largest expert count (256)
 __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
     const int32_t* __restrict__ idx, int T, int E_all, int e_lo, int E, int K, int bn_max, const uint4* __restrict__ x,
     int row_vecs, int* __restrict__ expert_offset, int4* __restrict__ tiles, int* __restrict__ tile_done,
-    int* __restrict__ perm_src, int* __restrict__ inv_slot, uint4* __restrict__ x_perm, int* status) {
+    int* __restrict__ perm_src, int* __restrict__ inv_slot, uint4* __restrict__ x_perm,
+    const uint4* __restrict__ side_src, int side_vecs, uint4* __restrict__ side_dst, int* status) {
     pdl_wait();
     pdl_trigger();
     __shared__ uint32_t bm[kSmallThreads * kSmallWords];
@@ -258,13 +269,19 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
         }
     }
     __syncthreads();
-    // gather: this block's share of the 16-byte pieces of the dispatched rows
-    const long long total = static_cast<long long>(total_rows) * row_vecs;
+    // gather: this block's share of the 16-byte pieces of the dispatched rows (and of the
+    // side rows, if any)
+    const long long main_total = static_cast<long long>(total_rows) * row_vecs;
+    const long long total = main_total + static_cast<long long>(total_rows) * side_vecs;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + tid; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int r = static_cast<int>(i / row_vecs);
-        const int v = static_cast<int>(i - static_cast<long long>(r) * row_vecs);
-        x_perm[i] = x[static_cast<size_t>(src_s[r]) * row_vecs + v];
+        const bool side = i >= main_total;
+        const long long j = side ? i - main_total : i;
+        const int w = side ? side_vecs : row_vecs;
+        const int r = static_cast<int>(j / w);
+        const int v = static_cast<int>(j - static_cast<long long>(r) * w);
+        if (side) side_dst[j] = side_src[static_cast<size_t>(src_s[r]) * w + v];
+        else x_perm[j] = x[static_cast<size_t>(src_s[r]) * w + v];
     }
 }
 
@@ -305,32 +322,40 @@ cudaError_t launch_dispatch_scatter(const Shape& s, int e_lo, int E_loc, const i
 
 cudaError_t launch_dispatch_small(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T, int bn_max,
                                   const bf16* x, int* expert_offset, int4* tiles, int* tile_done, int* perm_src,
-                                  int* inv_slot, bf16* x_perm, int* status, int num_sms, cudaStream_t st) {
+                                  int* inv_slot, bf16* x_perm, int* status, int num_sms, cudaStream_t st,
+                                  const void* side_src, int side_bytes, void* side_dst) {
     if (T > kSmallDispatchT || E_loc > kSmallThreads || s.top_k > 32) return cudaErrorInvalidValue;
     const int row_vecs = s.d / 8;
-    const long long total = static_cast<long long>(T) * s.top_k * row_vecs;
+    const int side_vecs = side_src ? side_bytes / 16 : 0;
+    const long long total = static_cast<long long>(T) * s.top_k * (row_vecs + side_vecs);
     long long blocks = (total + 4 * kSmallThreads - 1) / (4 * kSmallThreads);
     if (blocks > num_sms) blocks = num_sms;
     if (blocks < 1) blocks = 1;
     const cudaError_t le_ = launch_pdl(dispatch_small_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kSmallThreads),
                                        0, st, topk_idx, T, s.E, e_lo, E_loc, s.top_k, bn_max,
                                        reinterpret_cast<const uint4*>(x), row_vecs, expert_offset, tiles, tile_done,
-                                       perm_src, inv_slot, reinterpret_cast<uint4*>(x_perm), status);
+                                       perm_src, inv_slot, reinterpret_cast<uint4*>(x_perm),
+                                       reinterpret_cast<const uint4*>(side_src), side_vecs,
+                                       reinterpret_cast<uint4*>(side_dst), status);
     if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, const int* n_rows, int rows,
-                               bf16* x_perm, int* status, int num_sms, cudaStream_t st) {
+                               bf16* x_perm, int* status, int num_sms, cudaStream_t st, const void* side_src,
+                               int side_bytes, void* side_dst) {
     const int row_vecs = d / 8;
-    const long long total = static_cast<long long>(rows) * row_vecs;
+    const int side_vecs = side_src ? side_bytes / 16 : 0;
+    const long long total = static_cast<long long>(rows) * (row_vecs + side_vecs);
     long long blocks = (total + 255) / 256;
     const long long cap = static_cast<long long>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     const cudaError_t le_ = launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, reinterpret_cast<const uint4*>(x), row_vecs, T,
                                                                       perm_src, n_rows,
-                                                                      reinterpret_cast<uint4*>(x_perm), status);
+                                                                      reinterpret_cast<uint4*>(x_perm),
+                                                                      reinterpret_cast<const uint4*>(side_src), side_vecs,
+                                                                      reinterpret_cast<uint4*>(side_dst), status);
     if (le_ != cudaSuccess) return le_;
     return cudaGetLastError();
 }

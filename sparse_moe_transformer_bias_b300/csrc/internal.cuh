@@ -63,7 +63,13 @@ struct Shape {
 };
 
 // Device status codes written to the status word (first error wins).
-enum : int { kStatusOk = 0, kStatusBadExpert = 1, kStatusWaitTimeout = 2, kStatusBadIndex = 3 };
+enum : int {
+    kStatusOk = 0,
+    kStatusBadExpert = 1,
+    kStatusWaitTimeout = 2,
+    kStatusBadIndex = 3,
+    kStatusRange = 4  // an NVFP4 activation block beyond its first piece's range (clamped)
+};
 
 // One N-tile of the grouped GEMMs: `rows` consecutive permuted rows starting at `row0`,
 // all routed to expert `e`. The work list is int4 {e, row0, rows, 0} after an int4 header
@@ -101,12 +107,17 @@ cudaError_t launch_dispatch_scatter(const Shape& s, int e_lo, int E_loc, const i
 // Count, scan, scatter and gather in one launch for small batches (T <= kSmallDispatchT,
 // E_loc <= 256, top_k <= 32): the same outputs as the four launches.
 constexpr int kSmallDispatchT = 128;
+// A side array (side_src rows of side_bytes, a multiple of 16, per token) is gathered into
+// side_dst beside the token rows when given.
 cudaError_t launch_dispatch_small(const Shape& s, int e_lo, int E_loc, const int32_t* topk_idx, int T, int bn_max,
                                   const bf16* x, int* expert_offset, int4* tiles, int* tile_done, int* perm_src,
-                                  int* inv_slot, bf16* x_perm, int* status, int num_sms, cudaStream_t st);
-// x_perm[row] = x[perm_src[row]] for the *n_rows rows dispatched (rows: an upper bound).
+                                  int* inv_slot, bf16* x_perm, int* status, int num_sms, cudaStream_t st,
+                                  const void* side_src = nullptr, int side_bytes = 0, void* side_dst = nullptr);
+// x_perm[row] = x[perm_src[row]] for the *n_rows rows dispatched (rows: an upper bound), and
+// likewise for the side array when given.
 cudaError_t launch_gather_rows(const bf16* x, int d, int T, const int* perm_src, const int* n_rows, int rows,
-                               bf16* x_perm, int* status, int num_sms, cudaStream_t st);
+                               bf16* x_perm, int* status, int num_sms, cudaStream_t st, const void* side_src = nullptr,
+                               int side_bytes = 0, void* side_dst = nullptr);
 
 // ---------------------------------------------------------------- expert MLP (expert_mlp.cu)
 // Largest N-tile (token rows per tile) the expert kernel uses for a batch of T tokens.
@@ -144,14 +155,20 @@ struct Nvfp4Experts {
     const uint8_t* dbs;
     const float* dts;
 };
-// Largest N-tile of the NVFP4 expert kernel (its widened weights share TMEM with the
-// accumulators, so tiles stop at 128 rows).
-int gemm_bn_max_fp4(const Shape& s, int T);
-// The expert kernel on NVFP4 weights (expert_mlp.cu): the same items and outputs as
-// launch_expert_mlp, the weights widened exactly to BF16 on chip; d and I multiples of 256.
-cudaError_t launch_expert_mlp_nvfp4(const Shape& s, const Nvfp4Experts& q, const bf16* x_perm, int rows,
-                                    const int4* tiles, int* tile_done, int max_tiles, int bn_max, bf16* h, bf16* y,
-                                    int* status, int num_sms, cudaStream_t st);
+// NVFP4 expert weights on the block-scaled FP4 tensor cores (expert_mlp_nvf4.cu): the same
+// items and outputs as launch_expert_mlp. Activations enter the products as four NVFP4
+// pieces per row (E2M1 codes, E4M3 scale per 16 elements, piece p weighted 2^-3p): x4_perm
+// [rows][4][d/2] codes and xs_perm [rows][4][d/16] scales of the dispatched rows; the gate/up
+// epilogues write h's pieces to h4 [rows][4][I/2] and hs [rows][4][I/16]. N-tiles of at most
+// 32 token rows; d and I multiples of 256.
+int gemm_bn_max_nvf4(const Shape& s, int T);
+cudaError_t launch_expert_mlp_nvf4(const Shape& s, const Nvfp4Experts& q, const uint8_t* x4_perm,
+                                   const uint8_t* xs_perm, int rows, const int4* tiles, int* tile_done, int max_tiles,
+                                   int bn_max, uint8_t* h4, uint8_t* hs, bf16* y, int* status, int num_sms,
+                                   cudaStream_t st);
+// The four NVFP4 pieces of the T BF16 token rows of width d: x4 [T][4][d/2], xs [T][4][d/16].
+cudaError_t launch_act4_prep(const bf16* x, int d, int T, uint8_t* x4, uint8_t* xs, int* status, int num_sms,
+                             cudaStream_t st);
 // FP8 E4M3 expert weights on the FP8 tensor cores (expert_mlp_fp8.cu): the same items and
 // outputs as launch_expert_mlp. Activations enter the products as two E4M3 pieces per row
 // under a power-of-two row scale: x8_perm holds the dispatched pieces of x (per permuted

@@ -146,7 +146,7 @@ def test_launch_count_and_stage_timing():
     ran = {k for k, v in times.items() if v > 0}
     assert n == len(ran), (n, times)
     # the plain forward has no pre-norm; for T <= 128 one launch covers the whole dispatch
-    assert set(abi.STAGES) - ran <= {"pre_norm", "dispatch_scan", "dispatch_scatter", "gather", "fp8_prep"}, times
+    assert set(abi.STAGES) - ran <= {"pre_norm", "dispatch_scan", "dispatch_scatter", "gather", "act_prep"}, times
     assert {"router_logits", "router_select", "dispatch_count", "expert_mlp", "combine"} <= ran, times
 
 
