@@ -511,33 +511,40 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 sc0 = args.ds[it.tl.x];
                 sc1 = col1_ok ? sc0 : 0.0f;
             }
-            bool released = false;
-            for (int c0 = col_part * 8; c0 < it.tl.z; c0 += kTokStep) {
-                // token column c0 + j: its piece p product in accumulator column 4(c0 + j) + p
-                float va[8], vb[8];
-                {
-                    uint32_t a[32], b[32];
-                    ptx::tmem_ld16(t0 + 4 * c0, *reinterpret_cast<uint32_t(*)[16]>(a));
-                    ptx::tmem_ld16(t0 + 4 * c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
-                    ptx::tmem_ld16(t1 + 4 * c0, *reinterpret_cast<uint32_t(*)[16]>(b));
-                    ptx::tmem_ld16(t1 + 4 * c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(b + 16));
-                    ptx::tmem_wait_ld();
+            // Every accumulator value this warp needs goes to registers first (at most kGran
+            // granules of 8 tokens, each reduced over its pieces at once); the accumulators then
+            // go back to the MMAs while the arithmetic below runs.
+            constexpr int kGran = (kBNMax + kTokStep - 1) / kTokStep;
+            float vag[kGran][8], vbg[kGran][8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        va[j] = __uint_as_float(a[4 * j]) + 0.125f * __uint_as_float(a[4 * j + 1]) +
+            for (int g = 0; g < kGran; ++g) {
+                const int c0 = col_part * 8 + g * kTokStep;
+                if (c0 >= it.tl.z) break;  // warp-uniform
+                // token column c0 + j: its piece p product in accumulator column 4(c0 + j) + p
+                uint32_t a[32], b[32];
+                ptx::tmem_ld16(t0 + 4 * c0, *reinterpret_cast<uint32_t(*)[16]>(a));
+                ptx::tmem_ld16(t0 + 4 * c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
+                ptx::tmem_ld16(t1 + 4 * c0, *reinterpret_cast<uint32_t(*)[16]>(b));
+                ptx::tmem_ld16(t1 + 4 * c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(b + 16));
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    vag[g][j] = __uint_as_float(a[4 * j]) + 0.125f * __uint_as_float(a[4 * j + 1]) +
                                 0.015625f * __uint_as_float(a[4 * j + 2]) + 0.001953125f * __uint_as_float(a[4 * j + 3]);
-                        vb[j] = __uint_as_float(b[4 * j]) + 0.125f * __uint_as_float(b[4 * j + 1]) +
+                    vbg[g][j] = __uint_as_float(b[4 * j]) + 0.125f * __uint_as_float(b[4 * j + 1]) +
                                 0.015625f * __uint_as_float(b[4 * j + 2]) + 0.001953125f * __uint_as_float(b[4 * j + 3]);
-                    }
                 }
-                if (c0 + kTokStep >= it.tl.z) {
-                    // this warp's last read of the accumulators: hand them back to the MMAs
-                    // before the arithmetic below
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(bar(TEMPTY0 + s0));
-                    ptx::mbar_arrive(bar(TEMPTY0 + s1));
-                    released = true;
-                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(TEMPTY0 + s0));
+            ptx::mbar_arrive(bar(TEMPTY0 + s1));
+            tph ^= (1u << s0) | (1u << s1);
+#pragma unroll
+            for (int g = 0; g < kGran; ++g) {
+                const int c0 = col_part * 8 + g * kTokStep;
+                if (c0 >= it.tl.z) break;  // warp-uniform
+                const float (&va)[8] = vag[g];
+                const float (&vb)[8] = vbg[g];
                 const int n_live = it.tl.z - c0;  // tokens j < n_live are rows of the tile
                 const size_t prow0 = static_cast<size_t>(it.tl.y) + c0;
                 if (!it.down) {
@@ -604,12 +611,6 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                     }
                 }
             }
-            if (!released) {
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(TEMPTY0 + s0));
-                ptx::mbar_arrive(bar(TEMPTY0 + s1));
-            }
-            tph ^= (1u << s0) | (1u << s1);
             if (!it.down) {
                 // publish this warp's h pieces (read by TMA in other CTAs)
                 fence_proxy_async_global();
@@ -714,13 +715,12 @@ bool encode_bmaps_u8_plain(BMaps* b, const void* base, uint64_t rows, uint64_t c
 
 }  // namespace
 
-#ifndef BEAM_NVF4_BN_LARGE
-#define BEAM_NVF4_BN_LARGE 32
-#endif
-
+// N-tiles of 16 token rows (64 piece rows, four accumulators) while experts average at most
+// 8 rows, else 32 (128 piece rows: the two accumulators of one item fill TMEM beside the
+// scale factors; faster at 4096 tokens than 20-row tiles with four accumulators).
 int gemm_bn_max_nvf4(const Shape& s, int T) {
     const long long avg_rows = static_cast<long long>(T) * s.top_k / s.E;
-    return avg_rows <= 8 ? 16 : BEAM_NVF4_BN_LARGE;
+    return avg_rows <= 8 ? 16 : 32;
 }
 
 cudaError_t launch_act4_prep(const bf16* x, int d, int T, uint8_t* x4, uint8_t* xs, int* status, int num_sms,
@@ -764,7 +764,6 @@ cudaError_t launch_expert_mlp_nvf4(const Shape& s, const Nvfp4Experts& q, const 
     a.ds = q.dts;
     const int grid = mlp_grid(a, max_tiles, num_sms);
     if (bn_max <= 16) return launch_q4<16>(w, bx, bxs, bh, bhs, a, h4, hs, grid, st);
-    if (bn_max <= 20) return launch_q4<20>(w, bx, bxs, bh, bhs, a, h4, hs, grid, st);
     return launch_q4<32>(w, bx, bxs, bh, bhs, a, h4, hs, grid, st);
 }
 
