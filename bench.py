@@ -52,7 +52,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # entry when its kernel changes after the capture.
 TRAFFIC_RATIO = {("decode", "bf16"): 2521634560 / 2520514560, ("prefill", "bf16"): 2607164672 / 2642411520,
                  ("decode", "fp8"): 1266699776 / 1263534080, ("prefill", "fp8"): 1472596224 / 1385431040,
-                 ("decode", "nvfp4"): 716948736 / 711721344, ("prefill", "nvfp4"): 955522560 / 833618304}
+                 ("decode", "nvfp4"): 716516096 / 712049024}
+
+# Dense tensor rate of a contraction's own operand type over BF16's, from the nominal B300
+# figures (BF16 2.25, FP8 4.5, NVFP4 13.5 PFLOP/s dense): the tensor peak of the FP8 and
+# NVFP4 expert kernels is the measured BF16 burst rate times this ratio.
+PEAK_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0}
 
 
 def peaks():
@@ -145,7 +150,9 @@ def algorithmic(shape, T, n_touched, rows, fp8=False, fp4=False):
     """Algorithmic FLOPs and bytes of the whole layer and of the expert kernel (one launch:
     gate/up + SwiGLU and down over the touched experts' weights). FP8 experts: one byte
     per weight plus one FP32 scale per weight row. NVFP4 experts: half a byte per weight,
-    one byte of block scale per 16 weights and one FP32 tensor scale per matrix."""
+    one byte of block scale per 16 weights and one FP32 tensor scale per matrix; their
+    activations (x, h) move as four NVFP4 pieces (codes 2 bytes and scales 1/4 byte per
+    element) instead of BF16 rows."""
     d, I, E, K = shape.d, shape.I, shape.E, shape.top_k
     if fp4:
         w_bytes = n_touched * (3 * d * I // 2 + 3 * d * I // 16 + 3 * 4)
@@ -156,8 +163,9 @@ def algorithmic(shape, T, n_touched, rows, fp8=False, fp4=False):
     layer_flops = T * (K * 3 * 2 * d * I + 2 * d * E)
     layer_bytes = w_bytes + E * d * 4 + E * 4 + 2 * T * d * 2 + T * K * 8
     # weights once; x_perm read, h written and read back, y (BF16) written
+    act = 2 + 0.25 if fp4 else 2  # bytes per activation element moved
     mlp = {"flops": 2 * rows * d * I * 3,
-           "bytes": w_bytes + rows * d * 2 + 2 * rows * I * 2 + rows * d * 2}
+           "bytes": int(w_bytes + rows * d * act + 2 * rows * I * act + rows * d * 2)}
     return layer_flops, layer_bytes, {"expert_mlp": mlp}
 
 
@@ -225,18 +233,24 @@ def measure(name, shape, T, hot, steps, warmup, experts, device, flush, pk, e2e=
     dom = "expert_mlp"
     kf, kb = kern[dom]["flops"], kern[dom]["bytes"]
     t_dom = stage_ms[dom] * 1e-3
-    hbm_bound = kb / (pk["hbm_gbs"] * 1e9) >= kf / (pk["bf16_tflops"] * 1e12)
+    wdt = "nvfp4" if fp4 else "fp8" if fp8 else "bf16"
+    t_peak = pk["bf16_tflops"] * PEAK_RATIO[wdt]
+    hbm_bound = kb / (pk["hbm_gbs"] * 1e9) >= kf / (t_peak * 1e12)
     if hbm_bound:
-        roof = {"bound": "hbm", "achieved": kb / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": kb / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs, copy)"}
     else:
-        roof = {"bound": "tensor", "achieved": kf / t_dom / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": kf / t_dom / 1e12, "peak": t_peak, "unit": "TFLOP/s",
+                "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)" + (
+                    "" if wdt == "bf16" else f" x {PEAK_RATIO[wdt]:g}, the nominal {wdt.upper()}/BF16 dense ratio")}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = dom
     roof["algorithmic_bytes" if hbm_bound else "algorithmic_flops"] = kb if hbm_bound else kf
     roof["kernel_ms"] = stage_ms[dom]
-    ratio = TRAFFIC_RATIO.get((name, "nvfp4" if fp4 else "fp8" if fp8 else "bf16"))
+    ratio = TRAFFIC_RATIO.get((name, wdt))
     roof["traffic"] = int(ratio * kb) if ratio is not None and shape.n_group == 8 else None
-    roof["frac_of_sustained"] = (kf / t_dom / 1e12 / pk["bf16_tflops_sustained"]) if not hbm_bound else None
+    roof["frac_of_sustained"] = (kf / t_dom / 1e12 / (pk["bf16_tflops_sustained"] * PEAK_RATIO[wdt])
+                                 if not hbm_bound else None)
 
     res = {
         "value": T * steps / (total_ms * 1e-3),
@@ -294,7 +308,10 @@ def measure_e2e(shape, T, x, wr, b, wg, wu, wd, steps, warmup, flush):
     x_dev = torch.empty_like(x)
     out_dev = torch.empty((T, shape.d), dtype=torch.bfloat16, device=x.device)
     stream = torch.cuda.current_stream()
-    for _ in range(warmup):
+    # more untimed steps than the device-timed pass: the host path (pinned copies, pool
+    # allocations, the first synchronisations after the stage-timing pass) settles slower
+    for _ in range(max(warmup, 20)):
+        flush.zero_()
         moe.forward_host(x_host, wr, b, wg, wu, wd, shape, out_host=out_host, stream=stream)
     total = 0.0
     per_step = []
@@ -524,9 +541,7 @@ def main():
                        "expert_weights": {"bf16": "BF16", "fp8": "FP8 E4M3, per-row FP32 scales",
                                           "nvfp4": "NVFP4 (E2M1, E4M3 block scales, FP32 tensor scale)"}[args.weights]},
             "roofline": {**res["roofline"],
-                         "peak_source": (f"measured (MEASURED_PEAKS.json "
-                                         f"{'hbm_gbs, copy' if res['roofline']['bound'] == 'hbm' else 'bf16_tflops, burst'})")
-                         if pk_src == "measured" else "fallback"},
+                         "peak_source": res["roofline"]["peak_source"] if pk_src == "measured" else "fallback"},
             "layer_roofline": res["layer_roofline"],
             "stage_ms": res["stage_ms"],
             "n_touched_experts": res["n_touched_experts"],

@@ -1,5 +1,6 @@
-// Pieces shared by the persistent expert kernels (expert_mlp.cu: BF16 and widened weights;
-// expert_mlp_fp8.cu: FP8 tensor-core products): the kernel arguments, the work-item
+// Pieces shared by the persistent expert kernels (expert_mlp.cu: BF16 weights;
+// expert_mlp_fp8.cu: FP8 tensor-core products; expert_mlp_nvf4.cu: block-scaled FP4
+// tensor-core products): the kernel arguments, the work-item
 // decoding of the dispatch work list, the bounded cross-CTA wait and the host-side
 // argument and grid helpers.
 #pragma once
@@ -27,7 +28,8 @@ struct MlpArgs {
     int I, d;
     bf16* h;
     bf16* y;             // [rows, d] expert outputs (the dense MLP: its output)
-    const float* gs;     // FP8 weights: per-row scales of Wg, Wu [E, I] and Wd [E, d]
+    const float* gs;     // FP8 weights: per-row scales of Wg, Wu [E, I] and Wd [E, d];
+                         // NVFP4 weights: the tensor scales of Wg, Wu and Wd [E]
     const float* us;
     const float* ds;
     // FP8 tensor-core products only (null otherwise): token of each permuted row, the

@@ -3,8 +3,9 @@
 // Hardware paragraph: FP8 checkpoints; the weight-only reading W[r][c] = scale[r] *
 // e4m3(q[r][c]) with one FP32 scale per output row).
 //
-// Why: a tcgen05.mma of M = 128 costs about the same time whatever its N up to 128 (a
-// measured ~93 cycles on B300), and kind::f8f6f4 takes K = 32 per instruction against 16 for
+// Why: a tcgen05.mma of M = 128 costs about the same time whatever its N up to 128 (about
+// 100 cycles measured on B300, for kind::f16 and kind::f8f6f4 alike), and kind::f8f6f4 takes
+// K = 32 per instruction against 16 for
 // BF16. Weights read as FP8 codes straight from shared memory therefore need half the MMA
 // instructions per weight byte of codes widened to BF16, which is what lets the decode
 // kernel run at the HBM rate of one byte per weight.

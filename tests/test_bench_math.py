@@ -1,6 +1,7 @@
 """The benchmark's roofline arithmetic against its definitions (no GPU): layer FLOPs
 T * (top_k * 3 * 2 * d * I + 2 * d * E); bytes of the touched experts' weights once (BF16:
-2 bytes per weight; FP8: 1 byte per weight plus one FP32 scale per weight row), the router,
+2 bytes per weight; FP8: 1 byte per weight plus one FP32 scale per weight row; NVFP4: half a
+byte per weight, a scale byte per 16 and an FP32 scale per matrix), the router,
 bias, tokens in and out, and the routing outputs; the expert kernel's bytes add its
 activation traffic."""
 import bench
@@ -28,6 +29,24 @@ def test_fp8_bytes_count_codes_and_row_scales():
     per_expert8 = 3 * 5120 * 2560 + (2 * 2560 + 5120) * 4
     assert bytes16 - bytes8 == 89 * (3 * 5120 * 2560 * 2 - per_expert8)
     assert kern8["expert_mlp"]["bytes"] == 89 * per_expert8 + 128 * (5120 * 2 + 2 * 2560 * 2 + 5120 * 2)
+
+
+def test_nvfp4_bytes_count_codes_scales_and_activation_pieces():
+    """NVFP4: half a byte per weight, one E4M3 scale byte per 16 weights and one FP32 tensor
+    scale per matrix; x and h move as four NVFP4 pieces (2 bytes of codes and 1/4 byte of
+    scales per element), y as BF16."""
+    s = W.BEAM
+    _, bytes4, kern4 = bench.algorithmic(s, 16, 89, 128, fp4=True)
+    _, bytes16, _ = bench.algorithmic(s, 16, 89, 128)
+    per_expert4 = 3 * 5120 * 2560 // 2 + 3 * 5120 * 2560 // 16 + 3 * 4
+    assert per_expert4 == 22_118_412
+    assert bytes16 - bytes4 == 89 * (3 * 5120 * 2560 * 2 - per_expert4)
+    act = 128 * (5120 * 2.25 + 2 * 2560 * 2.25 + 5120 * 2)
+    assert kern4["expert_mlp"]["bytes"] == 89 * per_expert4 + int(act)
+
+
+def test_tensor_peaks_follow_the_operand_type():
+    assert bench.PEAK_RATIO == {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0}   # 2.25 / 4.5 / 13.5 PFLOP/s
 
 
 def test_single_process_helpers():
