@@ -18,7 +18,8 @@
 // s_p of its block (the largest E2M1 gap is 2) and s_p <= 1.125 max|r_p| / 6, so
 // |r_4| <= (1.125 / 6)^4 max|v| = 1.2e-3 of the block's largest magnitude (usually far less).
 // The pieces of token row j of a tile are the B operand's rows 4j .. 4j+3 and u_p their
-// UE4M3 block scales; one MMA of N = 4b gives all four partial products, and the epilogue
+// UE4M3 block scales; one MMA over the tile's piece rows (4 per token, rounded up to 16)
+// gives all four partial products of every token, and the epilogue
 // takes acc = sum_p g_p * D[:, 4c + p] per token column c, then the weight matrix's tensor
 // scale, SwiGLU (gate/up, which splits h into its pieces at once) or the BF16 expert output
 // (down). The first piece covers block maxima up to 6 * 448 = 2688; a larger one is clamped
@@ -31,16 +32,22 @@
 // kernel (expert_mlp.cu). Roles (one CTA per SM):
 //   warp 0 lane 0: scheduler + TMA producer: per stage (K = 256) the two weight code tiles
 //                  [128 rows x 128 bytes] (128-byte swizzle) and their block-scale tiles
-//                  [128 x 16 bytes], the tile's activation pieces [4b rows x 128 bytes] and
-//                  their block scales [4b x 16 bytes];
-//   warp 1:        TMEM; lane 0 issues the MMAs (M = 128, N = 4b, K = 64, A and B from
-//                  shared memory, scale factors from TMEM) once the stage's scales are there;
+//                  [128 x 16 bytes], the tile's activation piece rows [128 bytes each] and
+//                  their block scales [16 bytes each];
+//   warp 1:        TMEM; lane 0 issues the MMAs (M = 128, N = the piece rows, K = 64, A and
+//                  B from shared memory, scale factors from TMEM) once the stage's scales
+//                  are there;
 //   warps 2..9:    epilogue (two warps per TMEM lane quarter, alternate 8-token granules);
+//                  each reads all its accumulator columns into registers and hands the
+//                  accumulators back before its arithmetic;
 //   warps 10..13:  scale-factor writers, one per TMEM lane quarter: each copies the stage's
 //                  block scales from shared memory into TMEM in the layout the MMA reads
-//                  (matrix row r at column r / 32, lane r % 32, the four 16-element blocks of
-//                  a K = 64 step in the four bytes of the word; every lane quarter the same).
-#include <cstring>
+//                  (matrix row r at column r / 32 and lane r % 32 of a lane quarter, the four
+//                  16-element blocks of a K = 64 step in the four bytes of the word). Each of
+//                  the tensor core's four sub-partitions reads its own lane quarter: the
+//                  weights' scales only for its 32 rows, the activation pieces' scales for
+//                  every row (measured with a probe: scales left out of the other quarters
+//                  change no result).
 #include <type_traits>
 
 #include "expert_common.cuh"
@@ -425,20 +432,27 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 }
                 const uint8_t* st_base = smem + stage * C::kStage;
                 const uint32_t sf = tmem_base + lane_off + C::kSfBase + stage * C::kSfCols;
-                // weights: column t*16 + kk*4 + g holds row 32g + lane's blocks 4kk .. 4kk+3
+                // The tensor core's four sub-partitions each read scale factors from their own
+                // TMEM lane quarter: the weights' scales of row r (K step kk) only by the
+                // sub-partition of rows 32q .. 32q+31 (lane r, column kk*4 + r/32 of the
+                // tile's group), the activation pieces' scales of row r by every one (lane
+                // 32q + r % 32, column kk*4 + r/32). So this warp loads only its quarter's
+                // weight rows (one 16-byte row per lane and tile) but every piece row.
+                const int q = warp & 3;
                 uint32_t a[32];
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
+                for (int t = 0; t < 2; ++t) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(st_base + C::kOffS + t * C::kS + (32 * q + lane) * 16);
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(st_base + C::kOffS + t * C::kS + (32 * g + lane) * 16);
                         a[t * 16 + 0 * 4 + g] = w.x;
                         a[t * 16 + 1 * 4 + g] = w.y;
                         a[t * 16 + 2 * 4 + g] = w.z;
                         a[t * 16 + 3 * 4 + g] = w.w;
                     }
+                }
                 ptx::tmem_st32(sf, a);
-                // activation pieces: column 32 + kk*4 + g holds piece row 32g + lane
+                // column 32 + kk*4 + g holds piece row 32g + lane (zero past the tile's rows)
                 uint32_t b[16];
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
