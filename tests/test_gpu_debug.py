@@ -64,3 +64,17 @@ def test_other_entry_points_unchanged():
     assert torch.equal(a, p)
     a, p = _both(lambda: moe.dense_mlp(x, wg[0], wu[0], wd[0]))
     assert torch.equal(a, p)
+
+
+@pytest.mark.parametrize("T", [7, 300])
+def test_nvfp4_unchanged_by_poisoned_scratch(T):
+    """The NVFP4 block keeps its activation pieces, their scales and h's pieces in scratch;
+    piece rows past a tile's tokens (read as padding of the products) may hold the poison,
+    which must stay out of every stored value and out of the range check."""
+    shape = W.TINY
+    x = W.make_tokens(shape, T, 2, "cuda")
+    wr, b = W.make_router(shape, 2, "cuda")
+    q4 = W.make_experts_nvfp4(shape, 2, "cuda")
+    a, p = _both(lambda: moe.forward_nvfp4(x, wr, b, q4, shape))
+    assert not torch.isnan(p.float()).any()
+    assert torch.equal(a, p)
