@@ -170,4 +170,15 @@ def test_beam_nvfp4_parity(beam_fp4, name, T, n_check):
     tokens = W.sample_tokens(T, n_check, seed=2).numpy()
     if T > n_check:
         tokens = np.unique(np.concatenate([tokens, [T - 1]]))
-    run_and_check(shape, x, wr, b, beam_fp4, tokens, f"{name} nvfp4 T={T}")
+    cache = {}
+    run_and_check(shape, x, wr, b, beam_fp4, tokens, f"{name} nvfp4 T={T}", cache)
+    if T >= 64:
+        # the expert with the most rows is split over several N-tiles of at most 32 rows: one
+        # token every 16 of its rows hits each of them but the last, which its last row hits
+        idx, _ = moe.route(x, wr, b, shape)
+        idx = idx.cpu().numpy()
+        load = np.bincount(idx.ravel(), minlength=shape.E)
+        hottest = int(load.argmax())
+        rows = np.nonzero((idx == hottest).any(axis=1))[0]
+        pick = np.unique(np.concatenate([rows[::16], rows[-1:]]))
+        run_and_check(shape, x, wr, b, beam_fp4, pick, f"{name} nvfp4 expert {hottest} ({load.max()} rows)", cache)
