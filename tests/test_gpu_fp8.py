@@ -183,4 +183,15 @@ def test_beam_fp8_parity(beam_fp8, name, T, n_check):
     tokens = W.sample_tokens(T, n_check, seed=2).numpy()
     if T > n_check:
         tokens = np.unique(np.concatenate([tokens, [T - 1]]))
-    run_and_check(shape, x, wr, b, beam_fp8, tokens, f"{name} fp8 T={T}")
+    cache = {}
+    run_and_check(shape, x, wr, b, beam_fp8, tokens, f"{name} fp8 T={T}", cache)
+    if T >= 1024:
+        # the expert with the most rows is split evenly over N-tiles of at most 128 rows, all
+        # but the last holding more than 64: one token every 64 of its rows and its last
+        idx, _ = moe.route(x, wr, b, shape)
+        idx = idx.cpu().numpy()
+        load = np.bincount(idx.ravel(), minlength=shape.E)
+        hottest = int(load.argmax())
+        rows = np.nonzero((idx == hottest).any(axis=1))[0]
+        pick = np.unique(np.concatenate([rows[::64], rows[-1:]]))
+        run_and_check(shape, x, wr, b, beam_fp8, pick, f"{name} fp8 expert {hottest} ({load.max()} rows)", cache)
