@@ -85,7 +85,7 @@ struct Q4Cfg {
     // FULL (TMA), SFREADY (scales in TMEM), EMPTY (MMAs done) per stage; TFULL, TEMPTY per
     // slot; RFULL, REMPTY per ring entry; DRAIN.
     static constexpr int kNumBars = 3 * kStages + 2 * kSlots + 2 * kRing + 1;
-    static constexpr int kSmemBytes = 1024 + kStages * kStage + kNumBars * 8 + kRing * 4 + 16;
+    static constexpr int kSmemBytes = 1024 + kStages * kStage + kNumBars * 8 + kRing * 4 + 16 + kRing * 32 + 16;
     static_assert(kBRows % kBoxRows == 0 && kSfB <= 4, "piece rows in whole boxes, at most 128");
     static_assert(kStages >= 2, "pipeline needs two stages");
     static_assert(kOffB % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
@@ -170,6 +170,27 @@ __device__ __forceinline__ uint32_t piece_scale(float amax, float& s, float& inv
     return code;
 }
 
+// A work item as the scheduler decoded it, handed to the other roles with its id (so they
+// do not read the work list from global memory again).
+struct RingItem {
+    int4 tl;   // {expert, first row, rows, 0}
+    int tile;
+    int m;
+    int flags;  // bit 0: down item; bit 1: valid
+    int pad;
+};
+
+__device__ __forceinline__ MItem item_of(const RingItem& r) {
+    MItem it;
+    it.tl = r.tl;
+    it.tile = r.tile;
+    it.m = r.m;
+    it.n_t = 0;
+    it.down = (r.flags & 1) != 0;
+    it.ok = (r.flags & 2) != 0;
+    return it;
+}
+
 template <int kBNMax>
 __global__ void __launch_bounds__(kQ4Threads, 1)
     expert_mlp_nvf4_kernel(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ CUtensorMap tmWu,
@@ -184,7 +205,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
     volatile int* ring = reinterpret_cast<volatile int*>(bars + C::kNumBars);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring) + kRing);
+    RingItem* items = reinterpret_cast<RingItem*>((reinterpret_cast<uintptr_t>(ring + kRing) + 15) & ~uintptr_t(15));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(items + kRing);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     constexpr int FULL0 = 0, SFR0 = C::kStages, EMPTY0 = 2 * C::kStages, TFULL0 = 3 * C::kStages,
                   TEMPTY0 = TFULL0 + C::kSlots, RFULL0 = TEMPTY0 + C::kSlots, REMPTY0 = RFULL0 + kRing,
@@ -257,18 +279,29 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
             while (ok) {
                 const int id = next < n_total ? next : -1;
                 if (id >= 0) next = atomicAdd(args.next_item, 1);
+                MItem it;
+                it.ok = false;
+                if (id >= 0) it = decode(args, id, n_gu, n_tiles);
                 if (!ptx::mbar_wait(bar(REMPTY0 + rslot), rphase ^ 1, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 ring[rslot] = id;
-                ptx::mbar_arrive(bar(RFULL0 + rslot));
+                if (id >= 0) {
+                    RingItem r;
+                    r.tl = it.tl;
+                    r.tile = it.tile;
+                    r.m = it.m;
+                    r.flags = (it.down ? 1 : 0) | (it.ok ? 2 : 0);
+                    r.pad = 0;
+                    items[rslot] = r;
+                }
+                ptx::mbar_arrive(bar(RFULL0 + rslot));  // release: the id and item are visible to the waiters
                 if (++rslot == kRing) {
                     rslot = 0;
                     rphase ^= 1;
                 }
                 if (id < 0) break;
-                const MItem it = decode(args, id, n_gu, n_tiles);
                 if (!it.ok || it.tl.z > kBNMax) {
                     flag_status(status, kStatusBadIndex);
                     continue;
@@ -345,13 +378,13 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                     break;
                 }
                 const int id = ring[rslot];
+                const MItem it = item_of(items[rslot]);
                 ptx::mbar_arrive(bar(REMPTY0 + rslot));
                 if (++rslot == kRing) {
                     rslot = 0;
                     rphase ^= 1;
                 }
                 if (id < 0) break;
-                const MItem it = decode(args, id, n_gu, n_tiles);
                 if (!it.ok || it.tl.z > kBNMax) continue;
                 const int s0 = slot, s1 = (slot + 1) % C::kSlots;
                 if (!ptx::mbar_wait(bar(TEMPTY0 + s0), ((tph >> s0) & 1u) ^ 1u, abort_flag, kWaitLimitNs) ||
@@ -415,6 +448,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 break;
             }
             const int id = ring[rslot];
+            const MItem it = item_of(items[rslot]);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(REMPTY0 + rslot));
             if (++rslot == kRing) {
@@ -422,7 +456,6 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 rphase ^= 1;
             }
             if (id < 0) break;
-            const MItem it = decode(args, id, n_gu, n_tiles);
             if (!it.ok || it.tl.z > kBNMax) continue;
             const int k_chunks = it.down ? args.kc_dn : args.kc_gu;
             for (int kc = 0; kc < k_chunks; ++kc) {
@@ -496,6 +529,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 break;
             }
             const int id = ring[rslot];
+            const MItem it = item_of(items[rslot]);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(REMPTY0 + rslot));
             if (++rslot == kRing) {
@@ -503,7 +537,6 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 rphase ^= 1;
             }
             if (id < 0) break;
-            const MItem it = decode(args, id, n_gu, n_tiles);
             if (!it.ok || it.tl.z > kBNMax) continue;
             const int s0 = slot, s1 = (slot + 1) % C::kSlots;
             if (!ptx::mbar_wait(bar(TFULL0 + s0), (tph >> s0) & 1u, abort_flag, kWaitLimitNs) ||
