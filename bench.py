@@ -52,7 +52,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # entry when its kernel changes after the capture.
 TRAFFIC_RATIO = {("decode", "bf16"): 2521638912 / 2520514560, ("prefill", "bf16"): 2606890752 / 2642411520,
                  ("decode", "fp8"): 1266699776 / 1263534080, ("prefill", "fp8"): 1472596224 / 1385431040,
-                 ("decode", "nvfp4"): 716247552 / 712049024, ("prefill", "nvfp4"): 836870656 / 844104064}
+                 ("decode", "nvfp4"): 716357632 / 712049024, ("prefill", "nvfp4"): 836847616 / 844104064}
 
 # Dense tensor rate of a contraction's own operand type over BF16's, from the nominal B300
 # figures (BF16 2.25, FP8 4.5, NVFP4 13.5 PFLOP/s dense): the tensor peak of the FP8 and
