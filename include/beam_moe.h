@@ -157,9 +157,10 @@ BEAM_MOE_API int beam_moe_forward_fp8(const beam_moe_config *cfg, const __nv_bfl
  * output). Numerics: the products run on the block-scaled FP4 tensor cores with the codes
  * and block scales as they are and FP32 accumulation. Each activation row (x, and h in FP32
  * straight from SwiGLU) enters them as four NVFP4 pieces: per block of 16 elements, piece p
- * has the E4M3 scale u_p = the least E4M3 value >= 2^(3p) max|r_p| / 6 and the E2M1 codes of
- * r_p / (2^-3p u_p) rounded to nearest, r_0 = v, r_(p+1) = r_p - 2^-3p u_p e2m1(code); what
- * is left after four pieces is at most 1.2e-3 of the block's largest magnitude. The tensor
+ * has the E4M3 scale u_p = the least E4M3 value >= 4^p max|r_p| / 6 and the E2M1 codes of
+ * r_p / (4^-p u_p) rounded to nearest, r_0 = v, r_(p+1) = r_p - 4^-p u_p e2m1(code); what
+ * is left after four pieces is at most 1.2e-3 of the block's largest magnitude (above an
+ * absolute floor of 2^-15 from the smallest scales). The tensor
  * scale is applied to each accumulator. A block whose largest magnitude exceeds 2688 is
  * clamped and recorded in the device status word (code 4). d and I must be multiples of 256.
  * Pointers as for beam_moe_forward_fp8. */

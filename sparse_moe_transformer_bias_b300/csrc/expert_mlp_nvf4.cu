@@ -11,12 +11,16 @@
 //
 // Both operands of this product are NVFP4, so the activations (x for the gate/up product, h
 // for the down product) enter as four NVFP4 pieces per row. For each block of 16 consecutive
-// elements, with r_0 = v and g_p = 2^(-3p):
-//     u_p = the least E4M3 value >= max|r_p| * 2^(3p) / 6,   s_p = g_p * u_p,
+// elements, with r_0 = v and g_p = 4^(-p):
+//     u_p = the least E4M3 value >= max|r_p| * 4^p / 6,   s_p = g_p * u_p,
 //     q_p = e2m1(r_p / s_p),   r_(p+1) = r_p - s_p * q_p        (p = 0 .. 3)
 // so v = sum_p g_p * u_p * q_p + r_4 with every step exact in FP32. Each piece leaves at most
 // s_p of its block (the largest E2M1 gap is 2) and s_p <= 1.125 max|r_p| / 6, so
-// |r_4| <= (1.125 / 6)^4 max|v| = 1.2e-3 of the block's largest magnitude (usually far less).
+// |r_4| <= (1.125 / 6)^4 max|v| = 1.2e-3 of the block's largest magnitude (usually far less),
+// above the floor of the smallest scales (2^-9 * 4^-3). The factor 4 per piece keeps every
+// later scale below the first one (max|r_p| * 4^p / 6 <= 0.75^p max|v| / 6), so no piece
+// after the first runs into the E4M3 maximum; with 8 the worst case grows by 1.5 per piece
+// and blocks above about 1,100 can lose precision in the last pieces.
 // The pieces of token row j of a tile are the B operand's rows 4j .. 4j+3 and u_p their
 // UE4M3 block scales; one MMA over the tile's piece rows (4 per token, rounded up to 16)
 // gives all four partial products of every token, and the epilogue
@@ -61,6 +65,7 @@ constexpr int kSfWarps = 4;
 constexpr int kQ4Threads = 64 + 32 * kEpiWarps + 32 * kSfWarps;
 constexpr int kQStage = 256;  // K per stage: one 128-byte row of FP4 codes
 constexpr int kPieces = 4;
+constexpr int kPieceShift = 2;  // piece p is weighted 2^(-kPieceShift * p)
 
 template <int kBNMax>
 struct Q4Cfg {
@@ -155,18 +160,18 @@ __device__ __forceinline__ uint32_t e2m1_pair(float y0, float y1, float& v0, flo
 }
 
 // Piece p of a block whose remainder has largest magnitude amax: the E4M3 scale u (its code
-// returned), the piece's step s = 2^-3p u and 1 / s (0 for an all-zero remainder). `over`
+// returned), the piece's step s = 4^-p u and 1 / s (0 for an all-zero remainder). `over`
 // is set when the first piece needs a scale above 448.
 template <int p>
 __device__ __forceinline__ uint32_t piece_scale(float amax, float& s, float& inv, bool& over) {
-    constexpr float kUp = static_cast<float>(1 << (3 * p)) / 6.0f;
-    constexpr float kDown = 1.0f / static_cast<float>(1 << (3 * p));
+    constexpr float kUp = static_cast<float>(1 << (kPieceShift * p)) / 6.0f;
+    constexpr float kDown = 1.0f / static_cast<float>(1 << (kPieceShift * p));
     float u;
     bool o = false;
     const uint32_t code = e4m3_ceil(amax * kUp, u, o);
     if (p == 0 && o) over = true;
     s = u * kDown;
-    inv = u > 0.0f ? static_cast<float>(1 << (3 * p)) * __frcp_rn(u) : 0.0f;
+    inv = u > 0.0f ? static_cast<float>(1 << (kPieceShift * p)) * __frcp_rn(u) : 0.0f;
     return code;
 }
 
@@ -562,6 +567,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
             // granules of 8 tokens, each reduced over its pieces at once); the accumulators then
             // go back to the MMAs while the arithmetic below runs.
             constexpr int kGran = (kBNMax + kTokStep - 1) / kTokStep;
+            constexpr float kG1 = 1.0f / (1 << kPieceShift), kG2 = kG1 * kG1, kG3 = kG2 * kG1;  // piece weights
             float vag[kGran][8], vbg[kGran][8];
 #pragma unroll
             for (int g = 0; g < kGran; ++g) {
@@ -576,10 +582,10 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    vag[g][j] = __uint_as_float(a[4 * j]) + 0.125f * __uint_as_float(a[4 * j + 1]) +
-                                0.015625f * __uint_as_float(a[4 * j + 2]) + 0.001953125f * __uint_as_float(a[4 * j + 3]);
-                    vbg[g][j] = __uint_as_float(b[4 * j]) + 0.125f * __uint_as_float(b[4 * j + 1]) +
-                                0.015625f * __uint_as_float(b[4 * j + 2]) + 0.001953125f * __uint_as_float(b[4 * j + 3]);
+                    vag[g][j] = __uint_as_float(a[4 * j]) + kG1 * __uint_as_float(a[4 * j + 1]) +
+                                kG2 * __uint_as_float(a[4 * j + 2]) + kG3 * __uint_as_float(a[4 * j + 3]);
+                    vbg[g][j] = __uint_as_float(b[4 * j]) + kG1 * __uint_as_float(b[4 * j + 1]) +
+                                kG2 * __uint_as_float(b[4 * j + 2]) + kG3 * __uint_as_float(b[4 * j + 3]);
                 }
             }
             ptx::tc_fence_before();
