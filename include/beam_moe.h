@@ -135,7 +135,7 @@ BEAM_MOE_API int beam_moe_forward_host(const beam_moe_config *cfg, const __nv_bf
  * FP32 accumulation; each BF16 activation row (x, and h after its BF16 rounding) enters
  * them as two E4M3 pieces under one power-of-two row scale s, v = s p1 + (s/16) p2, which is
  * exact for every value within 2^-10 of the row's largest magnitude (smaller ones carry an
- * absolute error below 2^-22 of it); each accumulator is multiplied by its row's scale in
+ * absolute error of at most 2^-14 s, below 2.8e-7 of it); each accumulator is multiplied by its row's scale in
  * FP32 before SwiGLU (gate/up) or before rounding the expert output (down). All pointers are
  * device memory, 16-byte aligned, owned by the caller and only read (out is written); errors
  * as for beam_moe_forward_ex. */

@@ -16,7 +16,7 @@
 //     v = s * p1 + (s / 16) * p2,   p1 = e4m3(v / s),   p2 = e4m3((v - s * p1) * 16 / s).
 // A BF16 value has 8 significant bits; p1 keeps the top 4 and the remainder has at most 4,
 // so both pieces are exact for every value within 2^-10 of the row's largest (smaller ones
-// land in the E4M3 subnormal range: an absolute error below a * 2^-22). The pieces of token
+// land in the E4M3 subnormal range: an absolute error of at most 2^-14 s < 2.8e-7 a). The pieces of token
 // row j of a tile are the B operand's rows 2j and 2j + 1, so one MMA of N = 2b (b = the
 // tile's rows rounded up to 16) gives both partial products, and the epilogue takes
 // acc = s * (D[:, 2c] + D[:, 2c + 1] / 16)  per token column c, then the weight row's scale,
