@@ -127,3 +127,24 @@ def test_forward_fp8_arguments_checked(lib):
         bad[i] = FAKE + 4
         assert f(cfg, *bad, 4, FAKE, None) == abi.BEAM_MOE_ERR_ALIGN, name
     assert f(cfg, *args, 4, None, None) == abi.BEAM_MOE_ERR_ARG
+
+
+def test_forward_nvfp4_arguments_checked(lib):
+    f = lib.beam_moe_forward_nvfp4
+    cfg = ctypes.byref(cfg_of())
+    args = [FAKE] * 12
+    assert f(cfg, *args, 0, FAKE, None) == abi.BEAM_MOE_OK
+    for i, name in enumerate(["x", "router_w", "expert_bias", "w_gate_q", "gate_block_scale", "gate_tensor_scale",
+                              "w_up_q", "up_block_scale", "up_tensor_scale", "w_down_q", "down_block_scale",
+                              "down_tensor_scale"]):
+        bad = list(args)
+        bad[i] = None
+        assert f(cfg, *bad, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG, name
+        assert name in abi.beam_moe_last_error()
+        bad[i] = FAKE + 4
+        assert f(cfg, *bad, 4, FAKE, None) == abi.BEAM_MOE_ERR_ALIGN, name
+    assert f(cfg, *args, 4, None, None) == abi.BEAM_MOE_ERR_ARG
+    # the 16-element blocks of a 256-wide stage: d and I multiples of 256
+    assert f(ctypes.byref(cfg_of(d=384, I=256)), *args, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert "multiples of 256" in abi.beam_moe_last_error()
+    assert f(ctypes.byref(cfg_of(d=512, I=384)), *args, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
