@@ -148,3 +148,53 @@ def test_forward_nvfp4_arguments_checked(lib):
     assert f(ctypes.byref(cfg_of(d=384, I=256)), *args, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
     assert "multiples of 256" in abi.beam_moe_last_error()
     assert f(ctypes.byref(cfg_of(d=512, I=384)), *args, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+
+
+def test_forward_host_arguments_checked(lib):
+    f = lib.beam_moe_forward_host
+    cfg = ctypes.byref(cfg_of())
+    w = [FAKE] * 5  # router_w, expert_bias, w_gate, w_up, w_down
+    assert f(cfg, None, *w, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG and "x_host" in abi.beam_moe_last_error()
+    assert f(cfg, FAKE, *w, 4, None, None) == abi.BEAM_MOE_ERR_ARG and "out_host" in abi.beam_moe_last_error()
+    assert f(cfg, FAKE, *w, -1, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert f(ctypes.byref(cfg_of(top_k=0)), FAKE, *w, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert f(cfg, FAKE, *w, 0, FAKE, None) == abi.BEAM_MOE_OK
+
+
+def test_rmsnorm_arguments_checked(lib):
+    f = lib.beam_moe_rmsnorm
+    eps = ctypes.c_float(1e-6)
+    for d in (0, 6, 8192 + 4):
+        assert f(d, FAKE, FAKE, eps, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG, d
+    assert f(5120, None, FAKE, eps, 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert f(5120, FAKE, FAKE + 8, eps, 4, FAKE, None) == abi.BEAM_MOE_ERR_ALIGN
+    assert f(5120, FAKE, FAKE, ctypes.c_float(float("nan")), 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert f(5120, FAKE, FAKE, ctypes.c_float(-1.0), 4, FAKE, None) == abi.BEAM_MOE_ERR_ARG
+    assert f(5120, FAKE, FAKE, eps, 0, FAKE, None) == abi.BEAM_MOE_OK
+
+
+def test_sublayer_arguments_checked(lib):
+    f = lib.beam_moe_sublayer_forward
+    cfg = ctypes.byref(cfg_of())
+    eps = ctypes.c_float(1e-6)
+
+    def call(stream_in=FAKE, pre=FAKE, post=FAKE, e=eps, k=5, T=4, out=FAKE, c=cfg):
+        return f(c, stream_in, pre, post, e, k, FAKE, FAKE, FAKE, FAKE, FAKE, T, out, None)
+
+    assert call(pre=None) == abi.BEAM_MOE_ERR_ARG and "pre_gamma" in abi.beam_moe_last_error()
+    assert call(post=None) == abi.BEAM_MOE_ERR_ARG and "post_gamma" in abi.beam_moe_last_error()
+    assert call(stream_in=None) == abi.BEAM_MOE_ERR_ARG and "stream_in" in abi.beam_moe_last_error()
+    assert call(out=None) == abi.BEAM_MOE_ERR_ARG and "stream_out" in abi.beam_moe_last_error()
+    assert call(k=1) == abi.BEAM_MOE_ERR_ARG and "k=1" in abi.beam_moe_last_error()
+    assert call(e=ctypes.c_float(float("inf"))) == abi.BEAM_MOE_ERR_ARG
+    assert call(c=ctypes.byref(cfg_of(d=8192 + 128))) == abi.BEAM_MOE_ERR_ARG
+    assert call(T=0) == abi.BEAM_MOE_OK
+
+
+@pytest.mark.parametrize("arg", ["x", "router_w", "expert_bias", "topk_idx", "topk_w"])
+def test_route_beam_shape_pointers_checked(lib, arg):
+    args = dict(x=FAKE, router_w=FAKE, expert_bias=FAKE, topk_idx=FAKE, topk_w=FAKE)
+    args[arg] = None
+    assert lib.beam_moe_route(args["x"], args["router_w"], args["expert_bias"], 4, args["topk_idx"],
+                              args["topk_w"], None) == abi.BEAM_MOE_ERR_ARG
+    assert arg in abi.beam_moe_last_error()
